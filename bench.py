@@ -1,0 +1,422 @@
+"""Benchmark of the forward-convolution library on GB300.
+
+Default workload: the detection-stem layer (conv2d fp32, N=1, IC=3, 640x640,
+OC=32, k=3, pad 1, stride 2, bias + ReLU): one step is one forward call
+through the C ABI (gbconv_conv2d_fwd) with inputs resident in HBM. L2 (129
+MB) is larger than the layer's 18 MB working set, so a 256 MiB buffer is
+written between timed steps, outside the timed events. The line also carries
+the per-layer TFLOP/s, GB/s and roofline fraction of all five layer shapes,
+an end-to-end number with host buffers, and the CPU oracle timed on the host
+cores as a baseline.
+
+Multi-GPU: each rank runs an independent replica of the workload on its own
+GPU (the layer is one problem; no data exchange), barrier + synchronize
+around the timed region, max time over ranks; value = FLOP of all ranks / that
+time ("scaling": "weak").
+
+`--impl reference` times the fp64 CPU oracle (the only reference
+implementation: the pages ship no runnable code) on the same layer, on the
+host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = ("conv TFLOP/s and % of roofline per layer shape at 1 GB300 "
+          "(vs CPU oracle)")
+WORKLOADS = {"detection_stem": 2, "tiny": 1, "text_line_batch": 3,
+             "wide_dense_f16": 4, "video_vae_conv3d_f16": 5}
+DEFAULT_WORKLOAD = "detection_stem"
+FLUSH_BYTES = 256 << 20
+SM_COUNT_FALLBACK = 152
+FP32_LANES_PER_SM = 128
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": float(p["hbm_gbs"]),
+                "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained",
+                                                     p["bf16_tflops"])),
+                "sm_max_mhz": float(p.get("sm_max_mhz", 2070.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+            "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
+
+
+def fp32_peak_tflops(pk, sms):
+    """CUDA-core FFMA peak: SMs x 128 lanes x 2 FLOP x max SM clock."""
+    return sms * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,"
+         "clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------- traffic table
+def recorded_traffic(kernel_file, key):
+    """DRAM bytes per launch from the committed ncu summary, or None when
+    that kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "implicit_gemm_convolution_conv_gb300", "csrc",
+                       kernel_file)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        f = line.split()
+        if len(f) == 3 and not line.startswith("#") and f[0] == key:
+            return int(f[1]) if f[2] == sha else None
+    return None
+
+
+# ---------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import implicit_gemm_convolution_conv_gb300 as gb
+    from implicit_gemm_convolution_conv_gb300.torch_ops import Conv, to_device
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count or SM_COUNT_FALLBACK
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed_calls(conv, reps, warm, do_flush=True):
+        for _ in range(warm):
+            conv()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for e0, e1 in evs:
+            if do_flush:
+                flush.zero_()
+            e0.record(stream)
+            conv()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    L = synthetic.LAYERS[WORKLOADS[args.workload]]
+    inp = synthetic.make_inputs(L)
+    x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
+    b = torch.from_numpy(inp.b).to(dev)
+    conv = Conv(x, w, b, L.stride, L.pad, L.relu)
+    launches = {gb.ALGO_DIRECT: 1, gb.ALGO_IGEMM_FFMA: 2,
+                gb.ALGO_IGEMM_TC: 3}[conv.algo]
+
+    # warm-up, then exactly K timed steps between barriers
+    for _ in range(args.warmup):
+        flush.zero_()
+        conv()
+    barrier()
+    evs = [(torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t_wall = time.perf_counter()
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            conv()
+            e1.record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    flops = L.flops()
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    avg_s = total_ms / args.steps * 1e-3
+    line = None
+    if rank == 0:
+        achieved = L.compulsory_bytes() / avg_s / 1e9
+        kernel_key = f"direct_conv_kernel:{L.name}"
+        roof = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": recorded_traffic("direct.cu", kernel_key),
+                "kernel": "direct_conv_kernel",
+                "algorithmic_bytes_per_launch": L.compulsory_bytes(),
+                "peak_source": pk["source"] + " (hbm_gbs, burst)"}
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if L.dtype == "f32" else L.dtype,
+            "data": "synthetic (seeded; shapes of the pages' layers)",
+            "config": {"workload": L.name, "N": L.N, "C": L.C, "D": L.D,
+                       "H": L.H, "W": L.W, "OC": L.OC, "k": L.k,
+                       "pad": L.pad, "stride": L.stride, "relu": L.relu,
+                       "algo": gb.algo_name(conv.algo),
+                       "l2": "256 MiB buffer written between timed steps, "
+                             "outside the timed events",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "gpu_launches": launches * args.steps,
+            "clocks": clk.summary(),
+            "wall_s_timed_region": round(t_wall, 4),
+        }
+    barrier()
+
+    if rank == 0:
+        # end to end: pinned host buffers, H2D of x, w, b and D2H of y inside
+        # the timed region, through the same C-ABI call
+        hx = torch.from_numpy(np.ascontiguousarray(inp.x)).pin_memory()
+        hw = torch.from_numpy(np.ascontiguousarray(inp.w)).pin_memory()
+        hb = torch.from_numpy(inp.b).pin_memory()
+        hy = torch.empty(conv.y.shape, dtype=conv.y.dtype).pin_memory()
+        reps = min(args.steps, 200)
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            w.copy_(hw, non_blocking=True)
+            b.copy_(hb, non_blocking=True)
+            conv()
+            hy.copy_(conv.y, non_blocking=True)
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / reps
+        line["e2e"] = {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 4),
+                       "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": hx.numel() * hx.element_size() +
+                       hw.numel() * hw.element_size() + hb.numel() * 4,
+                       "d2h_bytes_per_step": hy.numel() * hy.element_size(),
+                       "ms_per_step": round(e2e_ms, 5)}
+        if not args.skip_layers:
+            line["per_layer"] = per_layer(gb, Conv, to_device, torch, dev,
+                                          timed_calls, pk, sms)
+        if not args.skip_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(L, inp, budget_s=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
+    """TFLOP/s, GB/s and roofline fraction of every layer shape (median of
+    R flushed reps; OIHW weights packed inside the call, and pre-packed)."""
+    out = []
+    p32 = fp32_peak_tflops(pk, sms)
+    for idx, L in sorted(synthetic.LAYERS.items()):
+        inp = synthetic.make_inputs(L)
+        x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
+        b = torch.from_numpy(inp.b).to(dev)
+        reps = 20 if idx == 5 else 50
+        rec = {"layer": L.name, "flop": L.flops(),
+               "bytes": L.compulsory_bytes()}
+        for prepack in (False, True):
+            conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack)
+            ms = timed_calls(conv, reps, 3)
+            med = statistics.median(ms)
+            s = med * 1e-3
+            pc = p32 if L.dtype == "f32" else pk["bf16_tflops"]
+            t_ideal = max(L.flops() / (pc * 1e12),
+                          L.compulsory_bytes() / (pk["hbm_gbs"] * 1e9))
+            t_ideal_335 = max(L.flops() / (pc * 1e12),
+                              L.compulsory_bytes() / 3.35e12)
+            key = "prepacked" if prepack else "oihw"
+            rec[key] = {
+                "algo": gb.algo_name(conv.algo),
+                "median_us": round(med * 1e3, 3),
+                "p10_us": round(np.percentile(ms, 10) * 1e3, 3),
+                "p90_us": round(np.percentile(ms, 90) * 1e3, 3),
+                "tflops": round(L.flops() / s / 1e12, 3),
+                "gbs": round(L.compulsory_bytes() / s / 1e9, 1),
+                "roofline_frac": round(t_ideal / s, 4),
+                "roofline_frac_at_3.35TBs": round(t_ideal_335 / s, 4),
+                "bound": ("tensor" if L.dtype != "f32" else "fp32") if
+                L.flops() / (pc * 1e12) > L.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)
+                else "hbm",
+                "compute_peak_tflops": round(pc, 1),
+            }
+            warm = timed_calls(conv, 20, 2, do_flush=False)
+            rec[key]["median_us_l2_warm"] = round(statistics.median(warm) * 1e3, 3)
+            del conv
+        out.append(rec)
+        del x, w, b
+    return out
+
+
+def cpu_baseline(L, inp, budget_s=10.0):
+    """The oracle as it stands on the host cores, on the whole layer when
+    one call fits the budget, else on a sample of outputs."""
+    import oracle
+    threads = oracle.threads()
+    t0 = time.perf_counter()
+    oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+    one = time.perf_counter() - t0
+    if one <= budget_s / 2:
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s and reps < 1000:
+            oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+            reps += 1
+        dt = time.perf_counter() - t0
+        flop = L.flops() * reps
+        sample = f"whole layer, {reps} calls"
+    else:
+        total = int(np.prod(L.y_shape()))
+        n = max(1000, int(total * (budget_s / 2) / one))
+        idx = np.random.Generator(np.random.PCG64(1)).integers(0, total, n)
+        t0 = time.perf_counter()
+        oracle.conv_at(inp.x, inp.w, inp.b, idx, L.stride, L.pad, L.relu,
+                       L.dtype)
+        dt = time.perf_counter() - t0
+        flop = L.flops() * n / total
+        sample = f"{n} of {total} outputs"
+    return {"value": round(flop / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": threads, "kind": "oracle", "sample": sample,
+            "seconds": round(dt, 3)}
+
+
+# ----------------------------------------------------------- reference
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    L = synthetic.LAYERS[WORKLOADS[args.workload]]
+    inp = synthetic.make_inputs(L)
+    import oracle
+    threads = oracle.threads()
+    for _ in range(args.warmup):
+        oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+    dt = time.perf_counter() - t0
+    value = L.flops() * args.steps / dt / 1e12
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' layers)",
+            "config": {"workload": L.name, "parallelism": "host cores"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s",
+                             "cores": threads, "kind": "oracle",
+                             "sample": f"whole layer per step, {args.steps} steps"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--skip-layers", action="store_true")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        if args.steps > 50:
+            args.steps = 50       # keep the CPU run to a few minutes
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

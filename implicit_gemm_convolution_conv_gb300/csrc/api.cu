@@ -1,0 +1,348 @@
+// C ABI: descriptor validation, kernel choice, workspace layout, dispatch.
+//
+// Validation follows the fault-tolerance rules of
+// githubissues.com/ysh329/OpenCL-101/52 ("init fault tolerance" and the
+// uninitialised-activation bug case): every field is checked, unknown enum
+// values are rejected, and nothing is launched for a rejected call.
+#include <cstring>
+
+#include "internal.h"
+
+namespace gbconv {
+
+namespace {
+
+int64_t out_extent(int64_t in, int k, int pad, int stride) {
+    int64_t span = in + 2 * (int64_t)pad - k;
+    if (span < 0) return 0;
+    return span / stride + 1;
+}
+
+bool in_range(int v, int lo, int hi) { return v >= lo && v <= hi; }
+
+// Structural validation: shapes and enums only (no pointers).
+gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
+    if (!d) return GBCONV_ERR_NULL;
+    if (ndim != 2 && ndim != 3) return GBCONV_ERR_SHAPE;
+    if (d->reserved != 0) return GBCONV_ERR_RESERVED;
+    if (!in_range(d->dtype, GBCONV_F32, GBCONV_BF16)) return GBCONV_ERR_DTYPE;
+    if (!in_range(d->act, GBCONV_ACT_NONE, GBCONV_ACT_RELU)) return GBCONV_ERR_ACT;
+    if (!in_range(d->w_layout, GBCONV_W_OIHW, GBCONV_W_PACKED)) return GBCONV_ERR_LAYOUT;
+    if (!in_range(d->algo, GBCONV_ALGO_AUTO, GBCONV_ALGO_IGEMM_TC)) return GBCONV_ERR_ALGO;
+    const int dims[] = {d->N, d->C, d->D, d->H, d->W, d->OC};
+    for (int v : dims)
+        if (!in_range(v, 1, GBCONV_MAX_DIM)) return GBCONV_ERR_SHAPE;
+    if (ndim == 2 && d->D != 1) return GBCONV_ERR_SHAPE;
+    if (!in_range(d->k, 1, GBCONV_MAX_K)) return GBCONV_ERR_SHAPE;
+    if (!in_range(d->stride, 1, GBCONV_MAX_STRIDE)) return GBCONV_ERR_SHAPE;
+    if (!in_range(d->pad, 0, GBCONV_MAX_K)) return GBCONV_ERR_SHAPE;
+
+    Problem q{};
+    q.ndim = ndim;
+    q.N = d->N; q.C = d->C; q.D = d->D; q.H = d->H; q.W = d->W;
+    q.OC = d->OC; q.k = d->k; q.pad = d->pad; q.stride = d->stride;
+    q.kd = ndim == 3 ? d->k : 1;
+    q.pad_d = ndim == 3 ? d->pad : 0;
+    int64_t od = ndim == 3 ? out_extent(d->D, d->k, d->pad, d->stride) : 1;
+    int64_t oh = out_extent(d->H, d->k, d->pad, d->stride);
+    int64_t ow = out_extent(d->W, d->k, d->pad, d->stride);
+    if (od <= 0 || oh <= 0 || ow <= 0) return GBCONV_ERR_SHAPE;
+    q.OD = (int)od; q.OH = (int)oh; q.OW = (int)ow;
+    q.taps = q.kd * q.k * q.k;
+    q.in_vol = (int64_t)q.D * q.H * q.W;
+    q.out_vol = od * oh * ow;
+    q.x_elems = (int64_t)q.N * q.C * q.in_vol;
+    q.w_elems = (int64_t)q.OC * q.C * q.taps;
+    q.y_elems = (int64_t)q.N * q.OC * q.out_vol;
+    if (q.x_elems > GBCONV_MAX_ELEMS || q.w_elems > GBCONV_MAX_ELEMS ||
+        q.y_elems > GBCONV_MAX_ELEMS)
+        return GBCONV_ERR_SHAPE;
+    q.dtype = d->dtype; q.act = d->act; q.w_layout = d->w_layout;
+    q.elt = d->dtype == GBCONV_F32 ? 4 : 2;
+
+    // Kernel choice. Small reduction depth (IC * kvol) is bandwidth-bound
+    // work: the direct kernel. Otherwise an implicit GEMM: tensor cores for
+    // 16-bit storage, exact fp32 FMA on CUDA cores for fp32.
+    int algo = d->algo;
+    if (algo == GBCONV_ALGO_AUTO) {
+        if ((int64_t)q.C * q.taps <= 64 && direct_supported(q))
+            algo = GBCONV_ALGO_DIRECT;
+        else if (q.dtype != GBCONV_F32 && tc_supported(q))
+            algo = GBCONV_ALGO_IGEMM_TC;
+        else
+            algo = GBCONV_ALGO_IGEMM_FFMA;
+    }
+    q.algo = algo;
+    if (algo == GBCONV_ALGO_DIRECT && !direct_supported(q)) return GBCONV_ERR_ALGO;
+    if (algo == GBCONV_ALGO_IGEMM_TC && (q.dtype == GBCONV_F32 || !tc_supported(q)))
+        return GBCONV_ERR_ALGO;
+    *p = q;
+    return GBCONV_OK;
+}
+
+bool aligned(const void *ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+bool overlap(const void *a, size_t an, const void *b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+gbconv_status device_check() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GBCONV_ERR_UNSUPPORTED_DEVICE;
+    }
+    return gbconv_device_supported(dev) ? GBCONV_OK : GBCONV_ERR_UNSUPPORTED_DEVICE;
+}
+
+gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
+                      const void *w, const float *b, void *y, cudaStream_t s) {
+    Problem p;
+    gbconv_status st = build_problem(d, ndim, &p);
+    if (st != GBCONV_OK) return st;
+    if (!x || !w || !y) return GBCONV_ERR_NULL;
+    if (!aligned(x, p.elt) || !aligned(w, p.elt) || !aligned(y, p.elt) ||
+        (b && !aligned(b, 4)))
+        return GBCONV_ERR_ALIGN;
+    if (p.w_layout == GBCONV_W_PACKED && !aligned(w, 256)) return GBCONV_ERR_ALIGN;
+    const size_t xb = (size_t)p.x_elems * p.elt, yb = (size_t)p.y_elems * p.elt;
+    const size_t wb = p.w_layout == GBCONV_W_PACKED ? packed_weight_bytes(p)
+                                                    : (size_t)p.w_elems * p.elt;
+    Workspace ws = workspace_layout(p);
+    if (ws.total > 0) {
+        if (!d->workspace || d->workspace_bytes < ws.total) return GBCONV_ERR_WORKSPACE;
+        if (!aligned(d->workspace, 256)) return GBCONV_ERR_WORKSPACE;
+    }
+    if (overlap(y, yb, x, xb) || overlap(y, yb, w, wb) ||
+        overlap(y, yb, b, b ? (size_t)p.OC * 4 : 0) ||
+        overlap(y, yb, d->workspace, ws.total))
+        return GBCONV_ERR_OVERLAP;
+    st = device_check();
+    if (st != GBCONV_OK) return st;
+
+    char *wsp = static_cast<char *>(d->workspace);
+    cudaError_t e = cudaSuccess;
+    switch (p.algo) {
+    case GBCONV_ALGO_DIRECT:
+        // The direct kernel reads OIHW; its packed form is an OIHW copy.
+        e = launch_direct(p, x, w, b, y, s);
+        break;
+    case GBCONV_ALGO_IGEMM_FFMA: {
+        const void *wp = w;
+        if (p.w_layout == GBCONV_W_OIHW) {
+            e = launch_pack_ffma(p, w, wsp + ws.w_off, s);
+            wp = wsp + ws.w_off;
+        }
+        if (e == cudaSuccess) e = launch_igemm_ffma(p, x, wp, b, y, s);
+        break;
+    }
+    case GBCONV_ALGO_IGEMM_TC: {
+        const void *wp = w;
+        if (p.w_layout == GBCONV_W_OIHW) {
+            e = launch_pack_tc(p, w, wsp + ws.w_off, s);
+            wp = wsp + ws.w_off;
+        }
+        if (e == cudaSuccess) e = launch_to_channels_last(p, x, wsp + ws.x_off, s);
+        if (e == cudaSuccess) e = launch_igemm_tc(p, wsp + ws.x_off, wp, b, y, s);
+        break;
+    }
+    default:
+        return GBCONV_ERR_ALGO;
+    }
+    if (e == cudaErrorInvalidValue) return GBCONV_ERR_CUDA;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GBCONV_ERR_LAUNCH;
+    }
+    return GBCONV_OK;
+}
+
+}  // namespace
+
+size_t packed_weight_bytes(const Problem &p) {
+    switch (p.algo) {
+    case GBCONV_ALGO_DIRECT:
+        return (size_t)p.w_elems * p.elt;
+    case GBCONV_ALGO_IGEMM_FFMA:
+        return (size_t)p.taps * p.C * ffma_ocpad(p.OC) * p.elt;
+    case GBCONV_ALGO_IGEMM_TC:
+        return (size_t)p.taps * p.OC * tc_cpad(p.C) * p.elt;
+    }
+    return 0;
+}
+
+Workspace workspace_layout(const Problem &p) {
+    Workspace ws;
+    size_t off = 0;
+    if (p.algo == GBCONV_ALGO_IGEMM_TC) {
+        ws.x_off = off;
+        ws.x_bytes = (size_t)p.N * p.in_vol * tc_cpad(p.C) * p.elt;
+        off = align256(off + ws.x_bytes);
+    }
+    if (p.w_layout == GBCONV_W_OIHW && p.algo != GBCONV_ALGO_DIRECT) {
+        ws.w_off = off;
+        ws.w_bytes = packed_weight_bytes(p);
+        off = align256(off + ws.w_bytes);
+    }
+    ws.total = off;
+    return ws;
+}
+
+}  // namespace gbconv
+
+using namespace gbconv;
+
+extern "C" {
+
+gbconv_status gbconv_conv2d_fwd(const gbconv_desc *desc, const void *x,
+                                const void *w, const float *b, void *y,
+                                cudaStream_t stream) {
+    return forward(desc, 2, x, w, b, y, stream);
+}
+
+gbconv_status gbconv_conv3d_fwd(const gbconv_desc *desc, const void *x,
+                                const void *w, const float *b, void *y,
+                                cudaStream_t stream) {
+    return forward(desc, 3, x, w, b, y, stream);
+}
+
+gbconv_status gbconv_output_shape(const gbconv_desc *desc, int ndim, int *OD,
+                                  int *OH, int *OW) {
+    Problem p;
+    gbconv_status st = build_problem(desc, ndim, &p);
+    if (st != GBCONV_OK) return st;
+    if (!OD || !OH || !OW) return GBCONV_ERR_NULL;
+    *OD = p.OD; *OH = p.OH; *OW = p.OW;
+    return GBCONV_OK;
+}
+
+gbconv_status gbconv_workspace_size(const gbconv_desc *desc, int ndim,
+                                    size_t *bytes) {
+    Problem p;
+    gbconv_status st = build_problem(desc, ndim, &p);
+    if (st != GBCONV_OK) return st;
+    if (!bytes) return GBCONV_ERR_NULL;
+    *bytes = workspace_layout(p).total;
+    return GBCONV_OK;
+}
+
+gbconv_status gbconv_weight_packed_size(const gbconv_desc *desc, int ndim,
+                                        size_t *bytes) {
+    Problem p;
+    gbconv_status st = build_problem(desc, ndim, &p);
+    if (st != GBCONV_OK) return st;
+    if (!bytes) return GBCONV_ERR_NULL;
+    *bytes = packed_weight_bytes(p);
+    return GBCONV_OK;
+}
+
+gbconv_status gbconv_weight_pack(const gbconv_desc *desc, int ndim,
+                                 const void *w_oihw, void *w_packed,
+                                 cudaStream_t stream) {
+    Problem p;
+    gbconv_status st = build_problem(desc, ndim, &p);
+    if (st != GBCONV_OK) return st;
+    if (!w_oihw || !w_packed) return GBCONV_ERR_NULL;
+    if (!aligned(w_oihw, p.elt) || !aligned(w_packed, 256)) return GBCONV_ERR_ALIGN;
+    if (overlap(w_oihw, (size_t)p.w_elems * p.elt, w_packed, packed_weight_bytes(p)))
+        return GBCONV_ERR_OVERLAP;
+    st = device_check();
+    if (st != GBCONV_OK) return st;
+    cudaError_t e;
+    switch (p.algo) {
+    case GBCONV_ALGO_DIRECT:
+        e = cudaMemcpyAsync(w_packed, w_oihw, (size_t)p.w_elems * p.elt,
+                            cudaMemcpyDeviceToDevice, stream);
+        break;
+    case GBCONV_ALGO_IGEMM_FFMA:
+        e = launch_pack_ffma(p, w_oihw, w_packed, stream);
+        break;
+    default:
+        e = launch_pack_tc(p, w_oihw, w_packed, stream);
+        break;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GBCONV_ERR_LAUNCH;
+    }
+    return GBCONV_OK;
+}
+
+gbconv_status gbconv_select_algo(const gbconv_desc *desc, int ndim, int *algo) {
+    Problem p;
+    gbconv_status st = build_problem(desc, ndim, &p);
+    if (st != GBCONV_OK) return st;
+    if (!algo) return GBCONV_ERR_NULL;
+    *algo = p.algo;
+    return GBCONV_OK;
+}
+
+int gbconv_device_supported(int device) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (device < 0 || device >= n) return 0;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+const char *gbconv_status_string(gbconv_status s) {
+    switch (s) {
+    case GBCONV_OK: return "ok";
+    case GBCONV_ERR_NULL: return "null pointer";
+    case GBCONV_ERR_SHAPE: return "invalid shape";
+    case GBCONV_ERR_DTYPE: return "invalid dtype";
+    case GBCONV_ERR_ACT: return "invalid activation";
+    case GBCONV_ERR_ALIGN: return "misaligned pointer";
+    case GBCONV_ERR_WORKSPACE: return "workspace missing, short or misaligned";
+    case GBCONV_ERR_UNSUPPORTED_DEVICE: return "unsupported device (need compute capability 10.3)";
+    case GBCONV_ERR_LAUNCH: return "kernel launch failed";
+    case GBCONV_ERR_TIMEOUT: return "device-side wait timed out";
+    case GBCONV_ERR_ALGO: return "algorithm unknown or not applicable";
+    case GBCONV_ERR_LAYOUT: return "invalid weight layout";
+    case GBCONV_ERR_OVERLAP: return "output overlaps an input or the workspace";
+    case GBCONV_ERR_CUDA: return "CUDA call failed";
+    case GBCONV_ERR_RESERVED: return "reserved field not zero";
+    }
+    return "unknown status";
+}
+
+const char *gbconv_algo_name(int algo) {
+    switch (algo) {
+    case GBCONV_ALGO_AUTO: return "auto";
+    case GBCONV_ALGO_DIRECT: return "direct";
+    case GBCONV_ALGO_IGEMM_FFMA: return "igemm_ffma";
+    case GBCONV_ALGO_IGEMM_TC: return "igemm_tc";
+    }
+    return "unknown";
+}
+
+gbconv_status gbconv_check_device_error(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GBCONV_ERR_CUDA;
+    }
+    unsigned int code = 0;
+    if (read_and_clear_device_error(&code) != cudaSuccess) {
+        cudaGetLastError();
+        return GBCONV_ERR_CUDA;
+    }
+    return code ? GBCONV_ERR_TIMEOUT : GBCONV_OK;
+}
+
+gbconv_status gbconv_set_wait_limit_ns(uint64_t ns) {
+    if (ns == 0) return GBCONV_ERR_SHAPE;
+    set_wait_limit_ns(ns);
+    return GBCONV_OK;
+}
+
+}  // extern "C"

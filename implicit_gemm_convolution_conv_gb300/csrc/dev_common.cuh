@@ -1,0 +1,35 @@
+// Device helpers shared by all kernels: storage-type conversion and the fused
+// epilogue (bias, optional ReLU, rounding to the storage type).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace gbconv {
+
+template <typename T> struct Storage;
+template <> struct Storage<float> {
+    static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
+    static __device__ __forceinline__ float to_float(float v) { return v; }
+    static __device__ __forceinline__ float from_float(float v) { return v; }
+};
+template <> struct Storage<__half> {
+    static __device__ __forceinline__ float load(const __half *p) { return __half2float(__ldg(p)); }
+    static __device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ __half from_float(float v) { return __float2half_rn(v); }
+};
+template <> struct Storage<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) { return __bfloat162float(__ldg(p)); }
+    static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_float(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Fused epilogue (lpnh.cn/news/2745477 section 2.2: bias added at write-back;
+// section 4.4: ReLU fused into the same write): v = acc + b, then max(v, 0).
+__device__ __forceinline__ float epilogue(float acc, float bias, int relu) {
+    float v = acc + bias;
+    return relu ? fmaxf(v, 0.0f) : v;
+}
+
+}  // namespace gbconv

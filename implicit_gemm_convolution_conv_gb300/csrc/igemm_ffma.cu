@@ -1,0 +1,206 @@
+// Implicit-GEMM convolution on CUDA cores (exact fp32 FMA, any storage type).
+//
+// GEMM view of the convolution sum of lpnh.cn/news/2745477 section 2.2:
+//   M = N * OD * OH * OW output pixels,  N_gemm = OC,  K = kvol * IC,
+//   A[m][kk] = x at the input coordinate of output pixel m and tap/channel kk
+//              (zero where that coordinate is padding),
+//   B[kk][oc] = packed weights, row kk = tap * IC + ic,
+//   y[n][oc][pixel] = epilogue(sum_kk A[m][kk] * B[kk][oc]).
+// A is never materialised (no im2col buffer): each CTA gathers its A tile
+// straight from the NCHW/NCDHW input into shared memory. CTA tile BM x BN,
+// K step BK, two shared-memory stages with the next stage prefetched into
+// registers while the current one is multiplied; each thread accumulates an
+// 8 x 8 register tile (two 4-wide pixel groups x two 4-wide channel groups).
+#include "dev_common.cuh"
+#include "internal.h"
+
+namespace gbconv {
+namespace {
+
+constexpr int BM = 128, BN = 64, BK = 16, NT = 128;
+static_assert(BN == kFfmaOcAlign, "packed OC padding must match the CTA tile");
+
+struct FfmaArgs {
+    const void *x;
+    const void *wp;     // [taps][C][OCp]
+    const float *b;
+    void *y;
+    int C, D, H, W, OC, OCp;
+    int k, kd, stride, pad, pad_d;
+    int OD, OH, OW;
+    int64_t M, out_vol, in_hw;
+    int K;              // taps * C
+    int relu;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(NT) igemm_ffma_kernel(const FfmaArgs a) {
+    __shared__ __align__(16) float As[2][BK][BM];
+    __shared__ __align__(16) float Bs[2][BK][BN];
+
+    const T *x = static_cast<const T *>(a.x);
+    const T *wp = static_cast<const T *>(a.wp);
+    const int tid = threadIdx.x;
+    const int64_t m0 = (int64_t)blockIdx.x * BM;
+    const int n0 = blockIdx.y * BN;
+
+    // This thread gathers A column `tid` (one output pixel) for every kk.
+    const int64_t my_m = m0 + tid;
+    const bool m_ok = my_m < a.M;
+    int img = 0, od = 0, oh = 0, ow = 0;
+    if (m_ok) {
+        int64_t r = my_m;
+        img = (int)(r / a.out_vol); r -= (int64_t)img * a.out_vol;
+        od = (int)(r / ((int64_t)a.OH * a.OW)); r -= (int64_t)od * a.OH * a.OW;
+        oh = (int)(r / a.OW); ow = (int)(r - (int64_t)oh * a.OW);
+    }
+    const int id0 = od * a.stride - a.pad_d, ih0 = oh * a.stride - a.pad,
+              iw0 = ow * a.stride - a.pad;
+    const int64_t x_img = (int64_t)img * a.C * a.D * a.in_hw;
+    const int64_t c_stride = (int64_t)a.D * a.in_hw;
+
+    // B loader: row tid/8 of the stage, 8 consecutive output channels.
+    const int b_row = tid / 8, b_col = (tid % 8) * 8;
+
+    float a_reg[BK];
+    float b_reg[8];
+
+    auto gather = [&](int k0) {
+        // (tap, c) of kk = k0; advanced incrementally across the BK rows.
+        int tap = k0 / a.C, c = k0 - tap * a.C;
+#pragma unroll
+        for (int r = 0; r < BK; r++) {
+            float v = 0.0f;
+            if (m_ok && tap < a.kd * a.k * a.k) {
+                const int kx = tap % a.k, ky = (tap / a.k) % a.k, kz = tap / (a.k * a.k);
+                const int id = id0 + kz, ih = ih0 + ky, iw = iw0 + kx;
+                if (id >= 0 && id < a.D && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W)
+                    v = Storage<T>::load(x + x_img + c * c_stride + (int64_t)id * a.in_hw +
+                                         (int64_t)ih * a.W + iw);
+            }
+            a_reg[r] = v;
+            if (++c == a.C) { c = 0; ++tap; }
+        }
+        const int kk = k0 + b_row;
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+            b_reg[j] = kk < a.K ? Storage<T>::load(wp + (int64_t)kk * a.OCp + n0 + b_col + j) : 0.0f;
+    };
+    auto stash = [&](int buf) {
+#pragma unroll
+        for (int r = 0; r < BK; r++) As[buf][r][tid] = a_reg[r];
+        *reinterpret_cast<float4 *>(&Bs[buf][b_row][b_col]) =
+            make_float4(b_reg[0], b_reg[1], b_reg[2], b_reg[3]);
+        *reinterpret_cast<float4 *>(&Bs[buf][b_row][b_col + 4]) =
+            make_float4(b_reg[4], b_reg[5], b_reg[6], b_reg[7]);
+    };
+
+    const int tm = tid % 16, tn = tid / 16;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[i][j] = 0.0f;
+
+    const int ksteps = (a.K + BK - 1) / BK;
+    gather(0);
+    stash(0);
+    __syncthreads();
+    for (int ks = 0; ks < ksteps; ks++) {
+        const int cur = ks & 1;
+        if (ks + 1 < ksteps) gather((ks + 1) * BK);
+#pragma unroll
+        for (int kk = 0; kk < BK; kk++) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&As[cur][kk][tm * 4]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&As[cur][kk][64 + tm * 4]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][tn * 4]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[cur][kk][32 + tn * 4]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int j = 0; j < 8; j++) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        if (ks + 1 < ksteps) {
+            stash(cur ^ 1);
+            __syncthreads();
+        }
+    }
+
+    T *y = static_cast<T *>(a.y);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int64_t m = m0 + (i < 4 ? tm * 4 + i : 64 + tm * 4 + (i - 4));
+        if (m >= a.M) continue;
+        const int64_t im = m / a.out_vol, pix = m - im * a.out_vol;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int oc = n0 + (j < 4 ? tn * 4 + j : 32 + tn * 4 + (j - 4));
+            if (oc >= a.OC) continue;
+            const float bias = a.b ? __ldg(a.b + oc) : 0.0f;
+            y[(im * a.OC + oc) * a.out_vol + pix] =
+                Storage<T>::from_float(epilogue(acc[i][j], bias, a.relu));
+        }
+    }
+}
+
+// wp[(tap * C + c) * OCp + oc] = w[(oc * C + c) * taps + tap], zero-padded in oc.
+template <typename T>
+__global__ void pack_ffma_kernel(const T *__restrict__ w, T *__restrict__ wp,
+                                 int OC, int C, int taps, int OCp) {
+    const int64_t total = (int64_t)taps * C * OCp;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int oc = (int)(e % OCp);
+        const int64_t kk = e / OCp;
+        const int c = (int)(kk % C), tap = (int)(kk / C);
+        wp[e] = oc < OC ? w[((int64_t)oc * C + c) * taps + tap] : T(0.0f);
+    }
+}
+
+template <typename T>
+cudaError_t launch_ffma_typed(const FfmaArgs &a, cudaStream_t s) {
+    dim3 grid((unsigned)((a.M + BM - 1) / BM), (a.OC + BN - 1) / BN);
+    igemm_ffma_kernel<T><<<grid, NT, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_pack_typed(const Problem &p, const void *w, void *wp, cudaStream_t s) {
+    const int64_t total = (int64_t)p.taps * p.C * ffma_ocpad(p.OC);
+    const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+    pack_ffma_kernel<T><<<blocks, 256, 0, s>>>(static_cast<const T *>(w), static_cast<T *>(wp),
+                                               p.OC, p.C, p.taps, ffma_ocpad(p.OC));
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_igemm_ffma(const Problem &p, const void *x, const void *wp,
+                              const float *b, void *y, cudaStream_t s) {
+    FfmaArgs a{};
+    a.x = x; a.wp = wp; a.b = b; a.y = y;
+    a.C = p.C; a.D = p.D; a.H = p.H; a.W = p.W; a.OC = p.OC; a.OCp = ffma_ocpad(p.OC);
+    a.k = p.k; a.kd = p.kd; a.stride = p.stride; a.pad = p.pad; a.pad_d = p.pad_d;
+    a.OD = p.OD; a.OH = p.OH; a.OW = p.OW;
+    a.M = (int64_t)p.N * p.out_vol; a.out_vol = p.out_vol;
+    a.in_hw = (int64_t)p.H * p.W;
+    a.K = p.taps * p.C;
+    a.relu = p.act == GBCONV_ACT_RELU;
+    switch (p.dtype) {
+    case GBCONV_F32: return launch_ffma_typed<float>(a, s);
+    case GBCONV_F16: return launch_ffma_typed<__half>(a, s);
+    default: return launch_ffma_typed<__nv_bfloat16>(a, s);
+    }
+}
+
+cudaError_t launch_pack_ffma(const Problem &p, const void *w, void *wp, cudaStream_t s) {
+    switch (p.dtype) {
+    case GBCONV_F32: return launch_pack_typed<float>(p, w, wp, s);
+    case GBCONV_F16: return launch_pack_typed<__half>(p, w, wp, s);
+    default: return launch_pack_typed<__nv_bfloat16>(p, w, wp, s);
+    }
+}
+
+}  // namespace gbconv

@@ -1,0 +1,73 @@
+// Internal declarations shared by the host dispatcher and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gbconv.h"
+
+namespace gbconv {
+
+// A validated problem with every derived extent. Index math is int64.
+struct Problem {
+    int ndim;                 // 2 or 3
+    int N, C, D, H, W;        // D == 1 for 2D
+    int OC, k, pad, stride;
+    int kd;                   // kernel extent along D: k for 3D, 1 for 2D
+    int pad_d;                // pad along D: pad for 3D, 0 for 2D
+    int OD, OH, OW;
+    int dtype, act, w_layout, algo;   // algo resolved (never AUTO)
+    int taps;                 // kd * k * k
+    int64_t x_elems, w_elems, y_elems;
+    int64_t out_vol;          // OD * OH * OW
+    int64_t in_vol;           // D * H * W
+    int elt;                  // bytes per stored element
+};
+
+// Tensor-core path channel padding: channels-last copies and packed weights
+// carry C rounded up to a multiple of 8 (16-byte rows for TMA).
+inline int tc_cpad(int C) { return (C + 7) / 8 * 8; }
+// CUDA-core implicit GEMM packs OC rounded up to this multiple.
+constexpr int kFfmaOcAlign = 64;
+inline int ffma_ocpad(int OC) { return (OC + kFfmaOcAlign - 1) / kFfmaOcAlign * kFfmaOcAlign; }
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Packed-weight bytes for the resolved algorithm.
+size_t packed_weight_bytes(const Problem &p);
+// Workspace layout for the resolved algorithm (offsets are 256-B aligned).
+struct Workspace {
+    size_t x_off = 0, x_bytes = 0;   // channels-last x (tensor-core path)
+    size_t w_off = 0, w_bytes = 0;   // packed weights (when w_layout == OIHW)
+    size_t total = 0;
+};
+Workspace workspace_layout(const Problem &p);
+
+// Whether a kernel family can run a problem (shared-memory and box limits).
+bool direct_supported(const Problem &p);
+bool tc_supported(const Problem &p);
+
+// Kernel launchers (each returns a cudaError_t from the launch).
+cudaError_t launch_direct(const Problem &p, const void *x, const void *w_oihw,
+                          const float *b, void *y, cudaStream_t s);
+cudaError_t launch_igemm_ffma(const Problem &p, const void *x,
+                              const void *w_packed, const float *b, void *y,
+                              cudaStream_t s);
+cudaError_t launch_pack_ffma(const Problem &p, const void *w_oihw,
+                             void *w_packed, cudaStream_t s);
+cudaError_t launch_pack_tc(const Problem &p, const void *w_oihw,
+                           void *w_packed, cudaStream_t s);
+cudaError_t launch_to_channels_last(const Problem &p, const void *x,
+                                    void *x_cl, cudaStream_t s);
+// Returns cudaErrorInvalidValue when the tensor maps cannot be encoded.
+cudaError_t launch_igemm_tc(const Problem &p, const void *x_cl,
+                            const void *w_packed, const float *b, void *y,
+                            cudaStream_t s);
+
+// Device-side error word and wait limit (defined in igemm_tc.cu).
+uint64_t wait_limit_ns();
+void set_wait_limit_ns(uint64_t ns);
+cudaError_t read_and_clear_device_error(unsigned int *code);
+
+}  // namespace gbconv

@@ -1,0 +1,105 @@
+"""Torch-tensor front end of the C ABI: allocation and argument marshalling.
+
+PyTorch provides device memory and the stream; `forward` allocates the output
+and the workspace the library asks for, then calls gbconv_conv2d_fwd /
+gbconv_conv3d_fwd. No arithmetic happens here.
+"""
+import numpy as np
+import torch
+
+from . import (ACT_NONE, ACT_RELU, ALGO_AUTO, BF16, F16, F32, W_OIHW,
+               W_PACKED, GbconvError, check, conv2d_fwd, conv3d_fwd,
+               make_desc, select_algo, weight_pack, weight_packed_size,
+               workspace_size)
+
+TORCH_DTYPE = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
+CODE_OF = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+
+def to_device(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """numpy storage array -> torch tensor on `device` (bf16 from uint16 bits)."""
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+        return t.view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def to_numpy(t: torch.Tensor) -> np.ndarray:
+    """torch tensor -> numpy storage array (bf16 as uint16 bits)."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def _desc(x, OC, k, stride, pad, relu, algo, w_layout):
+    nsp = x.dim() - 2
+    if nsp == 2:
+        N, C, H, W = x.shape
+        D = 1
+    else:
+        N, C, D, H, W = x.shape
+    d = make_desc(N, C, H, W, OC, k=k, pad=pad, stride=stride, D=D,
+                  dtype=CODE_OF[x.dtype], act=ACT_RELU if relu else ACT_NONE,
+                  w_layout=w_layout, algo=algo)
+    return d, nsp
+
+
+def output_tensor(x, OC, k, stride, pad):
+    sp = [(n + 2 * pad - k) // stride + 1 for n in x.shape[2:]]
+    return torch.empty([x.shape[0], OC] + sp, dtype=x.dtype, device=x.device)
+
+
+class Conv:
+    """A prepared convolution: descriptor, output and workspace allocated once.
+
+    `w` is OIHW/OIDHW; with `prepack=True` it is packed once with
+    gbconv_weight_pack and later calls pass w_layout PACKED.
+    """
+
+    def __init__(self, x, w, b=None, stride=1, pad=0, relu=False,
+                 algo=ALGO_AUTO, prepack=False, out=None, workspace=None):
+        self.x, self.b = x, b
+        OC, k = w.shape[0], w.shape[-1]
+        layout = W_PACKED if prepack else W_OIHW
+        self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout)
+        st, self.algo = select_algo(self.desc, self.nsp)
+        check(st)
+        if prepack:
+            st, nb = weight_packed_size(self.desc, self.nsp)
+            check(st)
+            self.w = torch.empty(nb + 256, dtype=torch.uint8, device=x.device)
+            self.w = _aligned_view(self.w, nb)
+            check(weight_pack(self.desc, self.nsp, w, self.w))
+        else:
+            self.w = w
+        st, ws = workspace_size(self.desc, self.nsp)
+        check(st)
+        self.workspace_bytes = ws
+        if ws:
+            if workspace is None:
+                raw = torch.empty(ws + 256, dtype=torch.uint8, device=x.device)
+                workspace = _aligned_view(raw, ws)
+            self.desc.workspace = workspace.data_ptr()
+            self.desc.workspace_bytes = ws
+        self.workspace = workspace
+        self.y = out if out is not None else output_tensor(x, OC, k, stride, pad)
+        self._fn = conv2d_fwd if self.nsp == 2 else conv3d_fwd
+
+    def __call__(self, x=None, stream=None):
+        st = self._fn(self.desc, self.x if x is None else x, self.w, self.b,
+                      self.y, stream)
+        if st != 0:
+            raise GbconvError(st)
+        return self.y
+
+
+def _aligned_view(raw: torch.Tensor, nbytes: int) -> torch.Tensor:
+    off = (-raw.data_ptr()) % 256
+    return raw[off:off + nbytes]
+
+
+def forward(x, w, b=None, stride=1, pad=0, relu=False, algo=ALGO_AUTO,
+            prepack=False):
+    """One convolution call; returns y (allocated here)."""
+    return Conv(x, w, b, stride, pad, relu, algo, prepack)()

@@ -1,0 +1,196 @@
+/*
+ * gbconv: forward convolution (conv2d / conv3d, fused bias + ReLU) for one
+ * NVIDIA GB300 (sm_103a), exposed as a plain C ABI.
+ *
+ * The operation (lpnh.cn/news/2745477, PP-OCR on Vulkan compute shaders,
+ * section 2.2 "compute shader and SPIR-V"): every output element sums
+ * input x weight over all input channels and kernel taps, with the input
+ * coordinate derived from the output coordinate,
+ *     i = o*stride - pad + tap      (per spatial axis),
+ * taps outside the input contribute nothing (zero padding), and the bias of
+ * the output channel is added last. It is cross-correlation (no kernel flip).
+ * ReLU, when requested, is max(v, 0) applied after the bias, fused into the
+ * write-back as in section 4.4 of the same page. Convolution3D adds a frame
+ * (depth) axis with the same kernel size, pad and stride
+ * (git.erdda.com/Tencent/ncnn/discussions/7001, SeedVR2 NCNN Vulkan,
+ * section 3.2 "six custom layers").
+ *
+ * Output extent per axis: O = floor((I + 2*pad - k) / stride) + 1.
+ *
+ * Layouts (all densely packed, row-major, element offsets):
+ *   x  conv2d [N][C][H][W]        conv3d [N][C][D][H][W]
+ *   w  conv2d [OC][C][k][k]       conv3d [OC][C][k][k][k]   (w_layout OIHW)
+ *      or the opaque packed form written by gbconv_weight_pack (w_layout PACKED)
+ *   b  [OC], always float32, or NULL for no bias
+ *   y  conv2d [N][OC][OH][OW]     conv3d [N][OC][OD][OH][OW]
+ * x, w and y share the storage dtype (float32, float16 or bfloat16).
+ * Arithmetic: float32 accumulation on every path; float16/bfloat16 results are
+ * rounded to nearest-even from the float32 epilogue value.
+ *
+ * Ownership and memory: the caller owns every buffer (device memory). The
+ * library allocates nothing: paths that need scratch space take it from the
+ * caller's workspace (gbconv_workspace_size). x, w and b are read-only; y must
+ * not overlap them or the workspace.
+ *
+ * Streams: calls enqueue work on the caller's stream and return without
+ * synchronising; results are valid once the stream reaches that point. A
+ * forward call makes no allocation, no synchronisation and no host read of
+ * device data, so it can be recorded into a CUDA graph.
+ *
+ * Errors: every entry point returns a gbconv_status. Descriptors are validated
+ * completely (an unknown activation, dtype, layout or algorithm, a non-zero
+ * reserved field, a bad size, a NULL or misaligned pointer, overlapping
+ * buffers, a short workspace) before any CUDA call; a rejected call has no side
+ * effect. Nothing aborts the process.
+ */
+#ifndef GBCONV_H
+#define GBCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gbconv_status {
+    GBCONV_OK = 0,
+    GBCONV_ERR_NULL = 1,               /* a required pointer is NULL */
+    GBCONV_ERR_SHAPE = 2,              /* non-positive / oversized dims, empty output */
+    GBCONV_ERR_DTYPE = 3,              /* unknown storage dtype */
+    GBCONV_ERR_ACT = 4,                /* unknown activation */
+    GBCONV_ERR_ALIGN = 5,              /* pointer not aligned to its element size */
+    GBCONV_ERR_WORKSPACE = 6,          /* workspace missing, short or not 256-byte aligned */
+    GBCONV_ERR_UNSUPPORTED_DEVICE = 7, /* current device is not compute capability 10.3 */
+    GBCONV_ERR_LAUNCH = 8,             /* a kernel launch failed (cudaGetLastError) */
+    GBCONV_ERR_TIMEOUT = 9,            /* a bounded device-side wait ran out */
+    GBCONV_ERR_ALGO = 10,              /* unknown algorithm, or the forced one cannot run this shape */
+    GBCONV_ERR_LAYOUT = 11,            /* unknown weight layout */
+    GBCONV_ERR_OVERLAP = 12,           /* y overlaps x, w, b or the workspace */
+    GBCONV_ERR_CUDA = 13,              /* another CUDA runtime/driver call failed */
+    GBCONV_ERR_RESERVED = 14           /* a reserved descriptor field is not zero */
+} gbconv_status;
+
+typedef enum gbconv_dtype {
+    GBCONV_F32 = 0,
+    GBCONV_F16 = 1,
+    GBCONV_BF16 = 2
+} gbconv_dtype;
+
+typedef enum gbconv_act {
+    GBCONV_ACT_NONE = 0,
+    GBCONV_ACT_RELU = 1
+} gbconv_act;
+
+typedef enum gbconv_wlayout {
+    GBCONV_W_OIHW = 0,     /* [OC][C][k][k] or [OC][C][k][k][k] */
+    GBCONV_W_PACKED = 1    /* written by gbconv_weight_pack for the same desc */
+} gbconv_wlayout;
+
+/* Kernel families. AUTO picks by shape and dtype (see gbconv_select_algo). */
+typedef enum gbconv_algo {
+    GBCONV_ALGO_AUTO = 0,
+    GBCONV_ALGO_DIRECT = 1,      /* direct, shared-memory halo + register micro-tile (small IC*k^d) */
+    GBCONV_ALGO_IGEMM_FFMA = 2,  /* implicit GEMM on CUDA cores, exact fp32 FMA */
+    GBCONV_ALGO_IGEMM_TC = 3     /* implicit GEMM on tcgen05 tensor cores (fp16/bf16 storage) */
+} gbconv_algo;
+
+/*
+ * Problem descriptor. Zero-initialise it, then set every field you use.
+ * Kernel size, pad and stride are the same on every spatial axis (the pages'
+ * single kSize/pad/stride parameters). For conv2d, D must be 1.
+ */
+typedef struct gbconv_desc {
+    int N, C, D, H, W;        /* input: batch, channels, frames (1 for 2D), height, width */
+    int OC, k, pad, stride;   /* output channels, kernel size, zero pad, stride */
+    int dtype;                /* gbconv_dtype: storage type of x, w, y */
+    int act;                  /* gbconv_act */
+    int w_layout;             /* gbconv_wlayout */
+    int algo;                 /* gbconv_algo */
+    int reserved;             /* must be 0 */
+    void *workspace;          /* device scratch, >= gbconv_workspace_size bytes, 256-B aligned */
+    size_t workspace_bytes;
+} gbconv_desc;
+
+/* Limits enforced by validation. */
+#define GBCONV_MAX_DIM 65535      /* any of N, C, D, H, W, OC */
+#define GBCONV_MAX_K 16           /* kernel size */
+#define GBCONV_MAX_STRIDE 8
+#define GBCONV_MAX_ELEMS ((int64_t)1 << 36)   /* elements of x, w or y */
+
+/*
+ * Forward convolution, 2D. x, w, y: device pointers in the layouts above,
+ * aligned to their element size; b: device float32 [OC] or NULL. Enqueued on
+ * `stream`; returns before the work runs.
+ */
+gbconv_status gbconv_conv2d_fwd(const gbconv_desc *desc, const void *x,
+                                const void *w, const float *b, void *y,
+                                cudaStream_t stream);
+
+/* Forward convolution, 3D (Convolution3D over frames). Same contract. */
+gbconv_status gbconv_conv3d_fwd(const gbconv_desc *desc, const void *x,
+                                const void *w, const float *b, void *y,
+                                cudaStream_t stream);
+
+/* Output extents for ndim = 2 (OD = 1) or 3. Host only, no CUDA call. */
+gbconv_status gbconv_output_shape(const gbconv_desc *desc, int ndim, int *OD,
+                                  int *OH, int *OW);
+
+/*
+ * Bytes of caller workspace the forward call needs for this desc (0 when the
+ * chosen kernel needs none). Scratch holds the re-laid-out input (tensor-core
+ * path: channels-last copy of x) and, with w_layout OIHW, the packed weights.
+ * Host only.
+ */
+gbconv_status gbconv_workspace_size(const gbconv_desc *desc, int ndim,
+                                    size_t *bytes);
+
+/* Bytes of the packed weight buffer for this desc. Host only. */
+gbconv_status gbconv_weight_packed_size(const gbconv_desc *desc, int ndim,
+                                        size_t *bytes);
+
+/*
+ * Re-lay OIHW/OIDHW weights once into the form the chosen kernel reads, so
+ * that later calls can pass w_layout = PACKED and skip the per-call packing
+ * (the weights are re-arranged at export time, not in the hot path:
+ * lpnh.cn/news/2745477 sections 2.3 and 4.2). A pure permutation plus zero
+ * padding; bit-exact. w_packed must hold gbconv_weight_packed_size bytes and be
+ * 256-byte aligned. The packed form is only valid for a desc that selects the
+ * same algorithm, dtype, C, OC, k and ndim.
+ */
+gbconv_status gbconv_weight_pack(const gbconv_desc *desc, int ndim,
+                                 const void *w_oihw, void *w_packed,
+                                 cudaStream_t stream);
+
+/* The algorithm a forward call with this desc runs (resolves AUTO). Host only. */
+gbconv_status gbconv_select_algo(const gbconv_desc *desc, int ndim, int *algo);
+
+/* 1 if `device` is a compute capability 10.3 GPU this library can run on, else 0.
+   Never aborts, also on a machine without a GPU (cf. the backend-valid query
+   of githubissues.com/ysh329/OpenCL-101/52, "init fault tolerance"). */
+int gbconv_device_supported(int device);
+
+/* Static, human-readable name of a status / an algorithm. Never NULL. */
+const char *gbconv_status_string(gbconv_status status);
+const char *gbconv_algo_name(int algo);
+
+/*
+ * Synchronise `stream`, then read and clear the library's device error word
+ * for the current device. Returns GBCONV_ERR_TIMEOUT if a bounded wait inside
+ * a tensor-core kernel ran out since the last check (that kernel stopped
+ * early and its output is undefined), GBCONV_OK otherwise. Not for use inside
+ * stream capture.
+ */
+gbconv_status gbconv_check_device_error(cudaStream_t stream);
+
+/*
+ * Upper bound, in nanoseconds, on any single device-side wait inside the
+ * tensor-core kernel (default 2e9). Host only; affects later launches.
+ */
+gbconv_status gbconv_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GBCONV_H */

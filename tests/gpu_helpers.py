@@ -1,0 +1,80 @@
+"""Shared helpers of the GPU tests: run a layer through the C ABI and compare
+with the fp64 oracle at the tolerances the method's arithmetic allows.
+
+Tolerances (stated per storage dtype):
+  f32  : relative L2 error <= 1e-5 and max abs error <= 1e-4.
+  f16  : NRMSE = ||y - ref||_2 / ||ref||_2 <= 1e-3, and every element within
+         2^-10 |ref| + 3e-4 (one f16 ulp of the result plus fp32 accumulation).
+  bf16 : NRMSE <= 1e-3 against the exact result rounded to bf16 (bf16
+         rounding alone gives NRMSE ~1.5e-3 against the unrounded result),
+         NRMSE <= 2.5e-3 against the unrounded result, and every element
+         within 2^-7 |ref| + 3e-4.
+"""
+import numpy as np
+import torch
+
+import oracle
+import synthetic
+from implicit_gemm_convolution_conv_gb300 import ALGO_AUTO
+from implicit_gemm_convolution_conv_gb300.torch_ops import (Conv, to_device,
+                                                            to_numpy)
+
+
+def device_inputs(inp: synthetic.Inputs):
+    L = inp.layer
+    x = to_device(inp.x, L.dtype)
+    w = to_device(inp.w, L.dtype)
+    b = None if inp.b is None else torch.from_numpy(inp.b).cuda()
+    return x, w, b
+
+
+def run(inp: synthetic.Inputs, algo=ALGO_AUTO, prepack=False):
+    """Run the layer on the GPU; returns (y as float64 numpy, Conv)."""
+    L = inp.layer
+    x, w, b = device_inputs(inp)
+    conv = Conv(x, w, b, stride=L.stride, pad=L.pad, relu=L.relu, algo=algo,
+                prepack=prepack)
+    y = conv()
+    torch.cuda.synchronize()
+    return oracle.widen(to_numpy(y), L.dtype), conv
+
+
+def reference(inp: synthetic.Inputs, idx=None):
+    L = inp.layer
+    if idx is None:
+        return oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu,
+                           L.dtype)
+    return oracle.conv_at(inp.x, inp.w, inp.b, idx, L.stride, L.pad, L.relu,
+                          L.dtype)
+
+
+def errors(y, ref):
+    err = y - ref
+    nref = np.linalg.norm(ref)
+    return {"rel_l2": float(np.linalg.norm(err) / max(nref, 1e-300)),
+            "max_abs": float(np.max(np.abs(err))) if err.size else 0.0}
+
+
+def assert_close(dtype, y, ref, what=""):
+    y = np.asarray(y, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    assert y.shape == ref.shape
+    assert np.isfinite(y).all(), f"{what}: non-finite output"
+    e = errors(y, ref)
+    if dtype == "f32":
+        assert e["rel_l2"] <= 1e-5, (what, e)
+        assert e["max_abs"] <= 1e-4, (what, e)
+    elif dtype == "f16":
+        assert e["rel_l2"] <= 1e-3, (what, e)
+        bad = np.abs(y - ref) > 2.0 ** -10 * np.abs(ref) + 3e-4
+        assert not bad.any(), (what, e, int(bad.sum()), np.flatnonzero(bad)[:8])
+    elif dtype == "bf16":
+        ref_q = oracle.widen(synthetic.to_bf16_bits(ref), "bf16")
+        eq = errors(y, ref_q)
+        assert eq["rel_l2"] <= 1e-3, (what, eq)
+        assert e["rel_l2"] <= 2.5e-3, (what, e)
+        bad = np.abs(y - ref) > 2.0 ** -7 * np.abs(ref) + 3e-4
+        assert not bad.any(), (what, e, int(bad.sum()), np.flatnonzero(bad)[:8])
+    else:
+        raise ValueError(dtype)
+    return e

@@ -1,0 +1,179 @@
+"""C-ABI boundary tests that need no GPU.
+
+The library loads on a machine without a GPU, exports every entry point the
+header declares, lays out gbconv_desc as the C compiler does, and rejects
+every malformed descriptor with its status code before any CUDA call (a
+rejected call never touches the pointers it was given).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import implicit_gemm_convolution_conv_gb300 as gb
+import synthetic
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbconv.h")
+FAKE = 1 << 20          # a non-NULL, well-aligned address never dereferenced
+
+try:
+    import torch
+    HAVE_GPU = torch.cuda.is_available()
+except Exception:       # pragma: no cover
+    HAVE_GPU = False
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gbconv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    syms = declared_symbols()
+    assert len(syms) >= 12
+    assert sorted(gb.SYMBOLS) == syms
+    out = subprocess.run(["nm", "-D", "--defined-only", gb.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gbconv_\w+)", out))
+    for s in syms:
+        assert s in exported, s
+        assert hasattr(gb.LIB, s)
+
+
+def test_desc_layout_matches_c(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "gbconv.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(gbconv_desc),"
+        " offsetof(gbconv_desc, reserved), offsetof(gbconv_desc, workspace),"
+        " offsetof(gbconv_desc, workspace_bytes));return 0;}\n")
+    exe = tmp_path / "layout"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"),
+                            "include")
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                    str(src), "-o", str(exe)], check=True)
+    size, off_res, off_ws, off_wsb = map(int, subprocess.run(
+        [str(exe)], capture_output=True, text=True, check=True).stdout.split())
+    assert ctypes.sizeof(gb.Desc) == size
+    assert gb.Desc.reserved.offset == off_res
+    assert gb.Desc.workspace.offset == off_ws
+    assert gb.Desc.workspace_bytes.offset == off_wsb
+
+
+def _desc(**kw):
+    base = dict(N=1, C=3, H=32, W=32, OC=8, k=3, pad=1, stride=1)
+    base.update(kw)
+    return gb.make_desc(**base)
+
+
+BAD = [
+    (dict(N=0), gb.ERR_SHAPE), (dict(C=-1), gb.ERR_SHAPE),
+    (dict(H=0), gb.ERR_SHAPE), (dict(OC=0), gb.ERR_SHAPE),
+    (dict(k=0), gb.ERR_SHAPE), (dict(k=17), gb.ERR_SHAPE),
+    (dict(stride=0), gb.ERR_SHAPE), (dict(stride=9), gb.ERR_SHAPE),
+    (dict(pad=-1), gb.ERR_SHAPE), (dict(H=2, W=2, k=5, pad=0), gb.ERR_SHAPE),
+    (dict(D=2), gb.ERR_SHAPE),                       # conv2d needs D == 1
+    (dict(N=70000), gb.ERR_SHAPE),
+    (dict(N=4096, C=4096, H=4096, W=4096), gb.ERR_SHAPE),
+    (dict(dtype=3), gb.ERR_DTYPE), (dict(dtype=-1), gb.ERR_DTYPE),
+    (dict(act=2), gb.ERR_ACT), (dict(act=-7), gb.ERR_ACT),
+    (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=4), gb.ERR_ALGO),
+    (dict(reserved=1), gb.ERR_RESERVED),
+    (dict(algo=gb.ALGO_IGEMM_TC), gb.ERR_ALGO),     # tensor cores need 16-bit
+    (dict(C=64, algo=gb.ALGO_DIRECT, k=15, pad=7, H=64, W=64, OC=32),
+     gb.ERR_ALGO),                                  # halo does not fit smem
+]
+
+
+@pytest.mark.parametrize("kw,status", BAD)
+def test_invalid_desc_rejected_before_cuda(kw, status):
+    d = _desc(**kw)
+    assert gb.conv2d_fwd(d, FAKE, FAKE, FAKE, FAKE * 2, 0) == status
+    assert gb.workspace_size(d, 2)[0] == status
+    assert gb.select_algo(d, 2)[0] == status
+
+
+def test_pointer_checks():
+    d = _desc()
+    assert gb.conv2d_fwd(d, None, FAKE, None, FAKE * 2, 0) == gb.ERR_NULL
+    assert gb.conv2d_fwd(d, FAKE, None, None, FAKE * 2, 0) == gb.ERR_NULL
+    assert gb.conv2d_fwd(d, FAKE, FAKE, None, None, 0) == gb.ERR_NULL
+    assert gb.conv2d_fwd(d, FAKE + 2, FAKE, None, FAKE * 2, 0) == gb.ERR_ALIGN
+    assert gb.conv2d_fwd(d, FAKE, FAKE, FAKE + 2, FAKE * 2, 0) == gb.ERR_ALIGN
+    # y overlapping x
+    assert gb.conv2d_fwd(d, FAKE, FAKE * 4, None, FAKE + 64, 0) == gb.ERR_OVERLAP
+    # 16-bit: 2-byte alignment suffices for x, w, y
+    dh = _desc(dtype=gb.F16)
+    assert gb.conv2d_fwd(dh, FAKE + 1, FAKE, None, FAKE * 2, 0) == gb.ERR_ALIGN
+    # NULL descriptor
+    assert gb.LIB.gbconv_conv2d_fwd(None, FAKE, FAKE, None, FAKE * 2, 0) == gb.ERR_NULL
+
+
+def test_workspace_checks():
+    L = synthetic.LAYERS[4]
+    d = gb.make_desc(L.N, L.C, L.H, L.W, L.OC, L.k, L.pad, L.stride,
+                     dtype=gb.F16)
+    st, need = gb.workspace_size(d, 2)
+    assert st == gb.OK
+    Cp = (L.C + 7) // 8 * 8
+    x_cl = L.N * L.H * L.W * Cp * 2
+    w_pk = 9 * L.OC * Cp * 2
+    assert need == (x_cl + 255) // 256 * 256 + (w_pk + 255) // 256 * 256
+    assert gb.conv2d_fwd(d, FAKE, FAKE * 64, None, FAKE * 128, 0) == gb.ERR_WORKSPACE
+    d.workspace, d.workspace_bytes = FAKE * 256, need - 1
+    assert gb.conv2d_fwd(d, FAKE, FAKE * 64, None, FAKE * 128, 0) == gb.ERR_WORKSPACE
+    d.workspace, d.workspace_bytes = FAKE * 256 + 16, need
+    assert gb.conv2d_fwd(d, FAKE, FAKE * 64, None, FAKE * 128, 0) == gb.ERR_WORKSPACE
+    # pre-packed weights need no weight scratch
+    d.w_layout = gb.W_PACKED
+    assert gb.workspace_size(d, 2) == (gb.OK, (x_cl + 255) // 256 * 256)
+    assert gb.weight_packed_size(d, 2) == (gb.OK, w_pk)
+
+
+@pytest.mark.skipif(HAVE_GPU, reason="this check needs a machine without a GPU")
+def test_valid_desc_reaches_device_check_without_gpu():
+    """A fully valid call on a machine without a GPU returns
+    UNSUPPORTED_DEVICE and never crashes."""
+    d = _desc()
+    assert gb.conv2d_fwd(d, FAKE, FAKE * 4, FAKE * 8, FAKE * 16, 0) == \
+        gb.ERR_UNSUPPORTED_DEVICE
+    assert gb.device_supported(0) == 0
+    assert gb.device_supported(-1) == 0
+    assert gb.check_device_error(0) == gb.ERR_CUDA
+
+
+@pytest.mark.parametrize("idx", sorted(synthetic.LAYERS))
+def test_shapes_and_algorithm_of_the_five_layers(idx):
+    L = synthetic.LAYERS[idx]
+    d = gb.make_desc(L.N, L.C, L.H, L.W, L.OC, L.k, L.pad, L.stride, D=L.D,
+                     dtype=L.dtype)
+    st, (od, oh, ow) = gb.output_shape(d, L.ndim)
+    assert st == gb.OK
+    assert (od, oh, ow) == L.out_dims()
+    st, algo = gb.select_algo(d, L.ndim)
+    assert st == gb.OK
+    expect = {1: gb.ALGO_DIRECT, 2: gb.ALGO_DIRECT, 3: gb.ALGO_IGEMM_FFMA,
+              4: gb.ALGO_IGEMM_TC, 5: gb.ALGO_IGEMM_TC}[idx]
+    assert algo == expect, gb.algo_name(algo)
+
+
+def test_conv3d_shapes():
+    d = gb.make_desc(1, 4, 6, 7, 2, k=3, pad=1, stride=2, D=5)
+    assert gb.output_shape(d, 3) == (gb.OK, (3, 3, 4))
+    d1 = gb.make_desc(1, 4, 6, 7, 2, k=3, pad=0, stride=1, D=2)
+    assert gb.output_shape(d1, 3)[0] == gb.ERR_SHAPE   # frames < k, no pad
+    assert gb.output_shape(d1, 4)[0] == gb.ERR_SHAPE   # ndim must be 2 or 3
+
+
+def test_status_and_algo_names():
+    for s in range(0, 15):
+        assert gb.status_string(s) and gb.status_string(s) != "unknown status"
+    assert gb.status_string(99) == "unknown status"
+    assert [gb.algo_name(a) for a in range(4)] == [
+        "auto", "direct", "igemm_ffma", "igemm_tc"]
+    assert gb.set_wait_limit_ns(0) == gb.ERR_SHAPE
+    assert gb.set_wait_limit_ns(2_000_000_000) == gb.OK

@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every case runs on seeded synthetic inputs. The five layer shapes run at full
+size through the same call the bench times (AUTO kernel choice, OIHW weights
+packed in the call); the small full-size layers are compared element by
+element with the whole oracle output, the two tensor-core layers on a sample
+of outputs (all border classes plus random ones) that the oracle computes one
+by one. A sweep of small shapes spanning several tiles and ragged tails
+covers each kernel family, each storage dtype, 2D and 3D, odd sizes, k = 1/3/5,
+pad 0/1/2, stride 1/2/3, no bias, ReLU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import implicit_gemm_convolution_conv_gb300 as gb
+from implicit_gemm_convolution_conv_gb300.torch_ops import Conv, to_numpy
+from gpu_helpers import assert_close, device_inputs, reference, run
+
+pytestmark = pytest.mark.gpu
+
+A_DIRECT, A_FFMA, A_TC = gb.ALGO_DIRECT, gb.ALGO_IGEMM_FFMA, gb.ALGO_IGEMM_TC
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    assert gb.device_supported(torch.cuda.current_device()) == 1
+    yield
+    assert gb.check_device_error() == gb.OK
+
+
+# ------------------------------------------------------- the five layers
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_layer_full_output(idx):
+    L = synthetic.LAYERS[idx]
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp)
+    ref = reference(inp)
+    assert_close(L.dtype, y, ref, L.name)
+
+
+@pytest.mark.parametrize("idx,dtype", [(4, "f16"), (5, "f16"), (4, "bf16")])
+def test_layer_sampled_output(idx, dtype):
+    L = synthetic.layer(idx, dtype=dtype)
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp)
+    assert conv.algo == A_TC
+    idx_s = synthetic.sample_indices(L, 20000)
+    ref = reference(inp, idx_s)
+    assert_close(L.dtype, y.ravel()[idx_s], ref, L.name)
+
+
+# --------------------------------------------------------- shape sweep
+def _L(dtype="f32", N=1, C=3, D=1, H=9, W=11, OC=4, k=3, pad=1, stride=1,
+       relu=False, bias=True, ndim=2, seed=1):
+    return synthetic.Layer("sweep", N=N, C=C, D=D, H=H, W=W, OC=OC, k=k,
+                           pad=pad, stride=stride, dtype=dtype, relu=relu,
+                           ndim=ndim, x_dist="n01", w_dist="he",
+                           b_dist="u11" if bias else "none", seed=seed)
+
+
+SWEEP = [
+    # direct kernel: templated k3/s1, k3/s2 and generic k/s, narrow and wide
+    (A_DIRECT, _L(C=3, H=32, W=32, OC=8)),
+    (A_DIRECT, _L(C=3, H=33, W=65, OC=40, stride=2, relu=True)),
+    (A_DIRECT, _L(C=2, H=1, W=70, OC=5, k=3, pad=1)),
+    (A_DIRECT, _L(C=3, H=13, W=17, OC=16, k=5, pad=2, stride=3)),
+    (A_DIRECT, _L(C=4, H=6, W=9, OC=33, k=1, pad=0, bias=False)),
+    (A_DIRECT, _L(N=3, C=3, H=20, W=70, OC=24, k=3, pad=0, stride=1)),
+    (A_DIRECT, _L(C=2, D=4, H=7, W=9, OC=6, ndim=3)),
+    (A_DIRECT, _L(C=1, D=5, H=9, W=8, OC=20, ndim=3, stride=2, relu=True)),
+    (A_DIRECT, _L(dtype="f16", C=3, H=40, W=67, OC=32, stride=2)),
+    (A_DIRECT, _L(dtype="bf16", C=3, H=21, W=30, OC=8)),
+    # CUDA-core implicit GEMM: ragged M, N and K, strides, 3D
+    (A_FFMA, _L(N=2, C=20, H=9, W=13, OC=130, relu=True)),
+    (A_FFMA, _L(C=64, H=12, W=80, OC=128)),
+    (A_FFMA, _L(C=7, H=15, W=16, OC=9, k=5, pad=2, stride=2)),
+    (A_FFMA, _L(C=5, H=10, W=10, OC=70, k=1, pad=0, stride=3, bias=False)),
+    (A_FFMA, _L(C=6, D=5, H=6, W=7, OC=12, ndim=3)),
+    (A_FFMA, _L(C=3, D=6, H=7, W=5, OC=65, ndim=3, stride=2, pad=2)),
+    (A_FFMA, _L(dtype="f16", N=2, C=16, H=11, W=12, OC=40)),
+    (A_FFMA, _L(dtype="bf16", C=12, H=9, W=9, OC=17, relu=True)),
+    # tensor-core implicit GEMM: several tiles, ragged tails, partial
+    # channel blocks, OC tails, strides, k 1/3/5, 3D incl. a single frame
+    (A_TC, _L(dtype="f16", C=64, H=8, W=128, OC=64)),
+    (A_TC, _L(dtype="f16", N=2, C=72, H=5, W=150, OC=40, relu=True)),
+    (A_TC, _L(dtype="f16", C=3, H=20, W=20, OC=16)),
+    (A_TC, _L(dtype="f16", C=136, H=7, W=33, OC=300, bias=False)),
+    (A_TC, _L(dtype="f16", C=32, H=17, W=61, OC=48, k=5, pad=2)),
+    (A_TC, _L(dtype="f16", C=16, H=12, W=14, OC=24, k=1, pad=0)),
+    (A_TC, _L(dtype="f16", C=24, H=19, W=41, OC=32, stride=2)),
+    (A_TC, _L(dtype="f16", C=8, H=16, W=300, OC=16, stride=3, pad=2)),
+    (A_TC, _L(dtype="bf16", C=64, H=9, W=70, OC=128, relu=True)),
+    (A_TC, _L(dtype="f16", C=16, D=5, H=8, W=40, OC=32, ndim=3)),
+    (A_TC, _L(dtype="f16", C=32, D=1, H=10, W=12, OC=16, ndim=3)),
+    (A_TC, _L(dtype="bf16", C=8, D=6, H=9, W=10, OC=24, ndim=3, stride=2)),
+]
+
+
+@pytest.mark.parametrize("algo,L", SWEEP,
+                         ids=[f"{gb.algo_name(a)}-{i}" for i, (a, _) in enumerate(SWEEP)])
+def test_sweep(algo, L):
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp, algo=algo)
+    assert conv.algo == algo
+    assert_close(L.dtype, y, reference(inp), str(L))
+
+
+# -------------------------------------------------- packing, determinism
+@pytest.mark.parametrize("idx,algo", [(2, A_DIRECT), (3, A_FFMA), (4, A_TC)])
+def test_prepacked_weights_give_identical_output(idx, algo):
+    inp = synthetic.make_inputs(synthetic.LAYERS[idx])
+    y0, _ = run(inp, algo=algo)
+    y1, _ = run(inp, algo=algo, prepack=True)
+    y2, _ = run(inp, algo=algo)
+    np.testing.assert_array_equal(y0, y1)
+    np.testing.assert_array_equal(y0, y2)
+
+
+def test_weight_pack_is_a_permutation():
+    """Packed tensor-core weights: wp[tap][oc][c] = w[oc][c][tap], zero pad."""
+    L = _L(dtype="f16", C=12, OC=5, k=3)
+    inp = synthetic.make_inputs(L)
+    _, w, _ = device_inputs(inp)
+    d = gb.make_desc(1, 12, 9, 11, 5, 3, 1, 1, dtype=gb.F16, algo=A_TC)
+    st, nb = gb.weight_packed_size(d, 2)
+    assert st == gb.OK and nb == 9 * 5 * 16 * 2
+    wp = torch.zeros(nb // 2 + 128, dtype=torch.float16, device="cuda")
+    off = (-wp.data_ptr()) % 256 // 2
+    wp = wp[off:off + nb // 2]
+    assert gb.weight_pack(d, 2, w, wp) == gb.OK
+    got = to_numpy(wp).reshape(9, 5, 16)
+    ref = np.zeros((9, 5, 16), np.float16)
+    ref[:, :, :12] = inp.w.reshape(5, 12, 9).transpose(2, 0, 1)
+    np.testing.assert_array_equal(got, ref)
+
+
+# --------------------------------------------------------- API behaviour
+def test_guard_bands_untouched():
+    """Stores stay inside y: canary bands around it keep their bytes."""
+    for idx in (1, 3, 4):
+        L = synthetic.LAYERS[idx]
+        inp = synthetic.make_inputs(L)
+        x, w, b = device_inputs(inp)
+        ny = int(np.prod(L.y_shape()))
+        band = 4096
+        buf = torch.full((ny + 2 * band,), -7.0, dtype=x.dtype, device="cuda")
+        y = buf[band:band + ny].view(L.y_shape())
+        Conv(x, w, b, L.stride, L.pad, L.relu, out=y)()
+        torch.cuda.synchronize()
+        assert bool((buf[:band] == -7.0).all()) and bool((buf[-band:] == -7.0).all())
+
+
+def test_graph_capture_and_side_stream():
+    L = synthetic.LAYERS[4]
+    inp = synthetic.make_inputs(L)
+    x, w, b = device_inputs(inp)
+    conv = Conv(x, w, b, L.stride, L.pad, L.relu)
+    eager = conv().clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        conv.y.zero_()
+        conv(stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(conv.y, eager)
+    g = torch.cuda.CUDAGraph()
+    conv.y.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        conv()
+    conv.y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(conv.y, eager)
+
+
+def test_repeat_calls_do_not_grow_memory():
+    """Many back-to-back calls: no device memory growth (cf. the driver leak
+    found by million-iteration loops in githubissues.com/ysh329/OpenCL-101/52)."""
+    L = synthetic.LAYERS[2]
+    inp = synthetic.make_inputs(L)
+    x, w, b = device_inputs(inp)
+    conv = Conv(x, w, b, L.stride, L.pad, L.relu)
+    conv()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(10000):
+        conv()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert abs(free1 - free0) < (8 << 20)
+    assert gb.check_device_error() == gb.OK
+
+
+def test_runtime_errors_on_gpu():
+    L = synthetic.LAYERS[4]
+    inp = synthetic.make_inputs(L)
+    x, w, b = device_inputs(inp)
+    y = torch.empty(L.y_shape(), dtype=x.dtype, device="cuda")
+    d = gb.make_desc(L.N, L.C, L.H, L.W, L.OC, L.k, L.pad, L.stride, dtype=gb.F16)
+    assert gb.conv2d_fwd(d, x, w, b, y) == gb.ERR_WORKSPACE
+    d32 = gb.make_desc(1, 3, 8, 8, 4, 3, 1, 1, algo=A_TC)
+    assert gb.conv2d_fwd(d32, x, w, b, y) == gb.ERR_ALGO
+    assert gb.conv3d_fwd(d, x, w, b, y) in (gb.ERR_WORKSPACE, gb.ERR_SHAPE)
