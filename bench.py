@@ -217,15 +217,37 @@ def run_ours(args):
     avg_s = total_ms / args.steps * 1e-3
     line = None
     if rank == 0:
-        achieved = L.compulsory_bytes() / avg_s / 1e9
-        kernel_key = f"direct_conv_kernel:{L.name}"
-        roof = {"bound": "hbm", "achieved": round(achieved, 1),
-                "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": recorded_traffic("direct.cu", kernel_key),
-                "kernel": "direct_conv_kernel",
-                "algorithmic_bytes_per_launch": L.compulsory_bytes(),
-                "peak_source": pk["source"] + " (hbm_gbs, burst)"}
+        kernel, kfile = {gb.ALGO_DIRECT: ("direct_conv_kernel", "direct.cu"),
+                         gb.ALGO_IGEMM_FFMA: ("igemm_ffma_kernel", "igemm_ffma.cu"),
+                         gb.ALGO_IGEMM_TC: ("igemm_tc_kernel", "igemm_tc.cu")}[conv.algo]
+        kernel_key = f"{kernel}:{L.name}"
+        if conv.algo == gb.ALGO_DIRECT:
+            achieved = L.compulsory_bytes() / avg_s / 1e9
+            roof = {"bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / pk["hbm_gbs"], 4),
+                    "algorithmic_bytes_per_launch": L.compulsory_bytes(),
+                    "peak_source": pk["source"] + " hbm_gbs (burst copy)"}
+        elif conv.algo == gb.ALGO_IGEMM_FFMA:
+            p32 = fp32_peak_tflops(pk, sms)
+            achieved = L.flops() / avg_s / 1e12
+            roof = {"bound": "alu", "achieved": round(achieved, 3),
+                    "peak": round(p32, 2), "unit": "TFLOP/s",
+                    "frac": round(achieved / p32, 4),
+                    "algorithmic_flops_per_launch": L.flops(),
+                    "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+        else:
+            achieved = L.flops() / avg_s / 1e12
+            roof = {"bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(achieved / pk["bf16_tflops"], 4),
+                    "algorithmic_flops_per_launch": L.flops(),
+                    "peak_source": pk["source"] + " bf16_tflops (burst; fp16 dense rate equals bf16)"}
+        roof["traffic"] = recorded_traffic(kfile, kernel_key)
+        roof["kernel"] = kernel
+        roof["timed"] = ("one call = one launch" if launches == 1 else
+                         f"one call = {launches} launches (weight pack, "
+                         "layout pass, GEMM); times are per call")
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
