@@ -18,6 +18,8 @@ OK = 0
 ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ACT, ERR_ALIGN, ERR_WORKSPACE = 1, 2, 3, 4, 5, 6
 ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALGO = 7, 8, 9, 10
 ERR_LAYOUT, ERR_OVERLAP, ERR_CUDA, ERR_RESERVED = 11, 12, 13, 14
+ERR_TOO_LARGE = 15
+NOALLOC_SCRATCH_BYTES = 8 << 20
 F32, F16, BF16 = 0, 1, 2
 ACT_NONE, ACT_RELU = 0, 1
 W_OIHW, W_PACKED = 0, 1
@@ -28,7 +30,7 @@ SYMBOLS = ["gbconv_conv2d_fwd", "gbconv_conv3d_fwd", "gbconv_output_shape",
            "gbconv_weight_pack", "gbconv_select_algo",
            "gbconv_device_supported", "gbconv_status_string",
            "gbconv_algo_name", "gbconv_check_device_error",
-           "gbconv_set_wait_limit_ns"]
+           "gbconv_set_wait_limit_ns", "gbconv_conv_fwd_noalloc"]
 
 
 class Desc(ctypes.Structure):
@@ -71,6 +73,7 @@ def _load():
         "gbconv_algo_name": ([I], ctypes.c_char_p),
         "gbconv_check_device_error": ([P], I),
         "gbconv_set_wait_limit_ns": ([ctypes.c_uint64], I),
+        "gbconv_conv_fwd_noalloc": ([DP, I, P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -174,6 +177,14 @@ def check_device_error(stream=None):
 
 def set_wait_limit_ns(ns):
     return LIB.gbconv_set_wait_limit_ns(ns)
+
+
+def conv_fwd_noalloc(desc, ndim, x, w, b, y, stream=None):
+    """gbconv_conv_fwd_noalloc: no workspace, no allocation (scratch is a
+    fixed array inside the library); returns the status code."""
+    return LIB.gbconv_conv_fwd_noalloc(ctypes.byref(desc), ndim, _ptr(x),
+                                       _ptr(w), _ptr(b), _ptr(y),
+                                       _stream(stream))
 
 
 def check(status):

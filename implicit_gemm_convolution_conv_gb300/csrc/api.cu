@@ -161,6 +161,10 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
 
 }  // namespace
 
+gbconv_status make_problem(const gbconv_desc *d, int ndim, Problem *p) {
+    return build_problem(d, ndim, p);
+}
+
 size_t packed_weight_bytes(const Problem &p) {
     switch (p.algo) {
     case GBCONV_ALGO_DIRECT:
@@ -312,6 +316,7 @@ const char *gbconv_status_string(gbconv_status s) {
     case GBCONV_ERR_OVERLAP: return "output overlaps an input or the workspace";
     case GBCONV_ERR_CUDA: return "CUDA call failed";
     case GBCONV_ERR_RESERVED: return "reserved field not zero";
+    case GBCONV_ERR_TOO_LARGE: return "problem needs more scratch than the fixed no-allocation array holds";
     }
     return "unknown status";
 }

@@ -69,7 +69,8 @@ typedef enum gbconv_status {
     GBCONV_ERR_LAYOUT = 11,            /* unknown weight layout */
     GBCONV_ERR_OVERLAP = 12,           /* y overlaps x, w, b or the workspace */
     GBCONV_ERR_CUDA = 13,              /* another CUDA runtime/driver call failed */
-    GBCONV_ERR_RESERVED = 14           /* a reserved descriptor field is not zero */
+    GBCONV_ERR_RESERVED = 14,          /* a reserved descriptor field is not zero */
+    GBCONV_ERR_TOO_LARGE = 15          /* gbconv_conv_fwd_noalloc: scratch need exceeds its fixed array */
 } gbconv_status;
 
 typedef enum gbconv_dtype {
@@ -189,6 +190,35 @@ gbconv_status gbconv_check_device_error(cudaStream_t stream);
  * tensor-core kernel (default 2e9). Host only; affects later launches.
  */
 gbconv_status gbconv_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Forward convolution that allocates nothing and takes no workspace.
+ * The pages have no counterpart of this entry point; it is a service for
+ * callers that cannot obtain device memory themselves, e.g. code running
+ * while a stream is being captured into a CUDA graph (where cudaMalloc is
+ * not allowed), real-time loops that must never enter the allocator, or
+ * plain-C hosts without a caching allocator.
+ *
+ * It runs the CUDA-core implicit-GEMM path (any dtype, 2D or 3D by `ndim`)
+ * and keeps that path's only scratch, the packed weights, in a fixed device
+ * array inside the library of GBCONV_NOALLOC_SCRATCH_BYTES bytes, which every
+ * GPU that loads the library holds until the process exits.
+ *   desc      as for gbconv_conv2d_fwd; algo must be AUTO or IGEMM_FFMA,
+ *             w_layout must be OIHW, workspace fields are ignored.
+ *   x, w, b, y  caller-owned device pointers, as for gbconv_conv2d_fwd.
+ * Errors: the usual validation codes; GBCONV_ERR_TOO_LARGE when the packed
+ * weights (taps * C * roundup(OC, 64) elements) exceed the fixed array.
+ * All calls on a device share the array: calls whose kernels overlap on the
+ * GPU race, so serialise them on one stream. The array keeps the last call's
+ * contents; every call rewrites all of it that it reads. The first call on a
+ * device looks up the array's address (cudaGetSymbolAddress, that device
+ * current); make that first call before any stream capture.
+ */
+#define GBCONV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+gbconv_status gbconv_conv_fwd_noalloc(const gbconv_desc *desc, int ndim,
+                                      const void *x, const void *w,
+                                      const float *b, void *y,
+                                      cudaStream_t stream);
 
 #ifdef __cplusplus
 }
