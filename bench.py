@@ -141,6 +141,58 @@ def recorded_traffic(kernel_file, key):
     return None
 
 
+# ------------------------------------------------------------- rotation
+ROTATE_BYTES = 256 << 20     # > 2 x L2: a set is cold when it comes round again
+
+
+class Rotation:
+    """R copies of the layer's input/output buffers used in turn, so that no
+    step finds its x or y in L2 (R x set bytes >= 256 MiB); steps are
+    recorded into CUDA graphs of back-to-back forward calls."""
+
+    def __init__(self, torch, conv, rotate=True):
+        self.torch = torch
+        x = conv.x
+        set_bytes = (x.numel() + conv.y.numel()) * x.element_size()
+        r = max(1, -(-ROTATE_BYTES // set_bytes)) if rotate else 1
+        self.resident = r > 64 or not rotate
+        r = min(r, 64)
+        self.convs = [conv] + [conv.with_input(x.clone()) for _ in range(r - 1)]
+        self.i = 0
+        self.l2_note = (f"inputs rotated over {r} copies of x and y "
+                        f"({r * set_bytes / 2**20:.0f} MiB > L2)"
+                        if not self.resident else
+                        f"{r} cop{'y' if r == 1 else 'ies'} of a {set_bytes} B "
+                        "layer: L2-resident")
+
+    def eager_step(self):
+        self.convs[self.i % len(self.convs)]()
+        self.i += 1
+
+    def graphs(self, steps):
+        """CUDA graphs whose replay runs exactly `steps` calls in turn."""
+        torch = self.torch
+        r = len(self.convs)
+        full, tail = divmod(steps, r)
+        out = []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for j in range(n):
+                    self.convs[j]()
+            return g
+        if full:
+            g = capture(r)
+            out += [g] * full
+        if tail:
+            out.append(capture(tail))
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        return out
+
+
 # ---------------------------------------------------------------- ours
 def run_ours(args):
     import torch
@@ -188,26 +240,25 @@ def run_ours(args):
     conv = Conv(x, w, b, L.stride, L.pad, L.relu)
     launches = {gb.ALGO_DIRECT: 1, gb.ALGO_IGEMM_FFMA: 2,
                 gb.ALGO_IGEMM_TC: 3}[conv.algo]
+    rot = Rotation(torch, conv)
 
     # warm-up, then exactly K timed steps between barriers
     for _ in range(args.warmup):
-        flush.zero_()
-        conv()
+        rot.eager_step()
     barrier()
-    evs = [(torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    graphs = rot.graphs(args.steps)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
         t_wall = time.perf_counter()
-        for e0, e1 in evs:
-            flush.zero_()
-            e0.record(stream)
-            conv()
-            e1.record(stream)
+        e0.record(stream)
+        for g in graphs:
+            g.replay()
+        e1.record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
-    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    total_ms = sum(step_ms)
+    total_ms = e0.elapsed_time(e1)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -215,9 +266,12 @@ def run_ours(args):
     flops = L.flops()
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     avg_s = total_ms / args.steps * 1e-3
+    iso = timed_calls(conv, 50, 3)
     line = None
     if rank == 0:
-        kernel, kfile = {gb.ALGO_DIRECT: ("direct_conv_kernel", "direct.cu"),
+        stem = L.ndim == 2 and L.C <= 4 and L.k == 3 and L.stride in (1, 2)
+        kernel, kfile = {gb.ALGO_DIRECT: ("direct_stem_kernel", "direct_stem.cu") if stem
+                         else ("direct_conv_kernel", "direct.cu"),
                          gb.ALGO_IGEMM_FFMA: ("igemm_ffma_kernel", "igemm_ffma.cu"),
                          gb.ALGO_IGEMM_TC: ("igemm_tc_kernel", "igemm_tc.cu")}[conv.algo]
         kernel_key = f"{kernel}:{L.name}"
@@ -259,13 +313,15 @@ def run_ours(args):
                        "H": L.H, "W": L.W, "OC": L.OC, "k": L.k,
                        "pad": L.pad, "stride": L.stride, "relu": L.relu,
                        "algo": gb.algo_name(conv.algo),
-                       "l2": "256 MiB buffer written between timed steps, "
-                             "outside the timed events",
+                       "l2": rot.l2_note,
+                       "timing": "CUDA graph of back-to-back forward calls "
+                                 "replayed; events around all K steps",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof,
             "gpu_launches": launches * args.steps,
             "clocks": clk.summary(),
             "wall_s_timed_region": round(t_wall, 4),
+            "latency_us_isolated_call": round(statistics.median(iso) * 1e3, 3),
         }
     barrier()
 
@@ -312,45 +368,62 @@ def run_ours(args):
 
 
 def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
-    """TFLOP/s, GB/s and roofline fraction of every layer shape (median of
-    R flushed reps; OIHW weights packed inside the call, and pre-packed)."""
+    """TFLOP/s, GB/s and roofline fraction of every layer shape: average
+    call time of back-to-back calls on rotated buffers (graph replay), with
+    OIHW weights packed inside the call and with pre-packed weights; plus
+    the isolated latency of one eager call after an L2 flush, and the
+    back-to-back time with L2-resident buffers."""
     out = []
     p32 = fp32_peak_tflops(pk, sms)
     for idx, L in sorted(synthetic.LAYERS.items()):
         inp = synthetic.make_inputs(L)
         x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
         b = torch.from_numpy(inp.b).to(dev)
-        reps = 20 if idx == 5 else 50
         rec = {"layer": L.name, "flop": L.flops(),
                "bytes": L.compulsory_bytes()}
+        pc = p32 if L.dtype == "f32" else pk["bf16_tflops"]
+        t_c = L.flops() / (pc * 1e12)
+        t_m = L.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)
+        t_ideal = max(t_c, t_m)
+        t_ideal_335 = max(t_c, L.compulsory_bytes() / 3.35e12)
         for prepack in (False, True):
             conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack)
-            ms = timed_calls(conv, reps, 3)
-            med = statistics.median(ms)
-            s = med * 1e-3
-            pc = p32 if L.dtype == "f32" else pk["bf16_tflops"]
-            t_ideal = max(L.flops() / (pc * 1e12),
-                          L.compulsory_bytes() / (pk["hbm_gbs"] * 1e9))
-            t_ideal_335 = max(L.flops() / (pc * 1e12),
-                              L.compulsory_bytes() / 3.35e12)
+            rot = Rotation(torch, conv)
+            calls = 200 if idx <= 3 else (100 if idx == 4 else 40)
+            for _ in range(3):
+                rot.eager_step()
+            gs = rot.graphs(calls)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for g in gs:
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            s = e0.elapsed_time(e1) / calls * 1e-3
+            warm_rot = Rotation(torch, conv, rotate=False)
+            gw = warm_rot.graphs(calls)
+            e0.record()
+            for g in gw:
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            s_warm = e0.elapsed_time(e1) / calls * 1e-3
+            iso = timed_calls(conv, 20, 2)
             key = "prepacked" if prepack else "oihw"
             rec[key] = {
                 "algo": gb.algo_name(conv.algo),
-                "median_us": round(med * 1e3, 3),
-                "p10_us": round(np.percentile(ms, 10) * 1e3, 3),
-                "p90_us": round(np.percentile(ms, 90) * 1e3, 3),
+                "us_per_call": round(s * 1e6, 3),
                 "tflops": round(L.flops() / s / 1e12, 3),
                 "gbs": round(L.compulsory_bytes() / s / 1e9, 1),
                 "roofline_frac": round(t_ideal / s, 4),
                 "roofline_frac_at_3.35TBs": round(t_ideal_335 / s, 4),
-                "bound": ("tensor" if L.dtype != "f32" else "fp32") if
-                L.flops() / (pc * 1e12) > L.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)
-                else "hbm",
+                "bound": ("tensor" if L.dtype != "f32" else "fp32") if t_c > t_m else "hbm",
                 "compute_peak_tflops": round(pc, 1),
+                "l2": rot.l2_note,
+                "us_per_call_l2_resident": round(s_warm * 1e6, 3),
+                "us_isolated_call_median": round(statistics.median(iso) * 1e3, 3),
             }
-            warm = timed_calls(conv, 20, 2, do_flush=False)
-            rec[key]["median_us_l2_warm"] = round(statistics.median(warm) * 1e3, 3)
-            del conv
+            del conv, rot, warm_rot, gs, gw
         out.append(rec)
         del x, w, b
     return out
@@ -422,7 +495,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)

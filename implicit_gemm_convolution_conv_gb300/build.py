@@ -14,7 +14,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgbconv.so")
-SOURCES = ["api.cu", "direct.cu", "igemm_ffma.cu", "igemm_tc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "direct.cu", "direct_stem.cu", "igemm_ffma.cu", "igemm_tc.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -205,6 +205,7 @@ bool direct_supported(const Problem &p) {
 
 cudaError_t launch_direct(const Problem &p, const void *x, const void *w,
                           const float *b, void *y, cudaStream_t s) {
+    if (stem_supported(p)) return launch_direct_stem(p, x, w, b, y, s);
     DirectArgs a{};
     a.x = x; a.w = w; a.b = b; a.y = y;
     a.N = p.N; a.C = p.C; a.D = p.D; a.H = p.H; a.W = p.W; a.OC = p.OC;

@@ -46,11 +46,14 @@ Workspace workspace_layout(const Problem &p);
 
 // Whether a kernel family can run a problem (shared-memory and box limits).
 bool direct_supported(const Problem &p);
+bool stem_supported(const Problem &p);   // few-channel 3x3 direct kernel
 bool tc_supported(const Problem &p);
 
 // Kernel launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_direct(const Problem &p, const void *x, const void *w_oihw,
                           const float *b, void *y, cudaStream_t s);
+cudaError_t launch_direct_stem(const Problem &p, const void *x, const void *w_oihw,
+                               const float *b, void *y, cudaStream_t s);
 cudaError_t launch_igemm_ffma(const Problem &p, const void *x,
                               const void *w_packed, const float *b, void *y,
                               cudaStream_t s);

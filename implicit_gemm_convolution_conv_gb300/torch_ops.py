@@ -4,6 +4,8 @@ PyTorch provides device memory and the stream; `forward` allocates the output
 and the workspace the library asks for, then calls gbconv_conv2d_fwd /
 gbconv_conv3d_fwd. No arithmetic happens here.
 """
+import copy
+
 import numpy as np
 import torch
 
@@ -85,6 +87,14 @@ class Conv:
         self.workspace = workspace
         self.y = out if out is not None else output_tensor(x, OC, k, stride, pad)
         self._fn = conv2d_fwd if self.nsp == 2 else conv3d_fwd
+
+    def with_input(self, x):
+        """The same prepared call (descriptor, weights, workspace) on another
+        input tensor of the same shape, writing a new output tensor."""
+        c = copy.copy(self)
+        c.x = x
+        c.y = torch.empty_like(self.y)
+        return c
 
     def __call__(self, x=None, stream=None):
         st = self._fn(self.desc, self.x if x is None else x, self.w, self.b,

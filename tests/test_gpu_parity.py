@@ -74,6 +74,9 @@ SWEEP = [
     (A_DIRECT, _L(C=1, D=5, H=9, W=8, OC=20, ndim=3, stride=2, relu=True)),
     (A_DIRECT, _L(dtype="f16", C=3, H=40, W=67, OC=32, stride=2)),
     (A_DIRECT, _L(dtype="bf16", C=3, H=21, W=30, OC=8)),
+    (A_DIRECT, _L(C=4, H=18, W=36, OC=64, stride=2, pad=0, relu=True)),
+    (A_DIRECT, _L(C=1, N=2, H=7, W=44, OC=36, stride=1)),
+    (A_DIRECT, _L(dtype="f16", C=3, H=24, W=64, OC=16, stride=2)),
     # CUDA-core implicit GEMM: ragged M, N and K, strides, 3D
     (A_FFMA, _L(N=2, C=20, H=9, W=13, OC=130, relu=True)),
     (A_FFMA, _L(C=64, H=12, W=80, OC=128)),
