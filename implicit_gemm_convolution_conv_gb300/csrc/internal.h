@@ -29,7 +29,7 @@ struct Problem {
 // carry C rounded up to a multiple of 8 (16-byte rows for TMA).
 inline int tc_cpad(int C) { return (C + 7) / 8 * 8; }
 // CUDA-core implicit GEMM packs OC rounded up to this multiple.
-constexpr int kFfmaOcAlign = 64;
+constexpr int kFfmaOcAlign = 128;
 inline int ffma_ocpad(int OC) { return (OC + kFfmaOcAlign - 1) / kFfmaOcAlign * kFfmaOcAlign; }
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
