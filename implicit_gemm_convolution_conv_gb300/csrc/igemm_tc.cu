@@ -2,24 +2,25 @@
 //
 // GEMM view of the convolution sum (lpnh.cn/news/2745477 section 2.2; the
 // Convolution3D extension of git.erdda.com/Tencent/ncnn/discussions/7001
-// section 3.2):  M = output pixels of one (n, od) plane tile, N = output
-// channels, K = taps x input channels. For each tap (kd, ky, kx) the A
-// operand is the input shifted by that tap, which TMA fetches straight from a
-// channels-last copy of x as a {64 ch, BW px, BH rows, 1 frame, 1 image} box:
-// padding is TMA's out-of-bounds zero fill and the stride is TMA's element
-// stride, so no im2col buffer exists. The B operand is the weight slab of the
-// same tap, packed once as [tap][OC][C] (the page's "re-arrange weights at
-// export time", sections 2.3 and 4.2).
+// section 3.2): M = 128 output channels, N = up to 256 output pixels of one
+// (n, od) plane tile, K = taps x input channels. The A operand is the weight
+// slab of one tap, packed once as [tap][OC][C] (the page's "re-arrange
+// weights at export time", sections 2.3 and 4.2). The B operand is the input
+// shifted by that tap, which TMA fetches straight from a channels-last copy
+// of x as a {64 ch, BW px, BH rows, 1 frame, 1 image} box: padding is TMA's
+// out-of-bounds zero fill and the stride is TMA's element stride, so no
+// im2col buffer exists.
 //
 // Persistent kernel, one CTA per SM, tiles handed out round-robin. Roles
-// (192 threads): warp 0 lane 0 issues TMA loads into a STAGES-deep
+// (320 threads): warp 0 lane 0 issues TMA loads into a STAGES-deep
 // shared-memory ring; warp 1 owns TMEM and lane 0 issues tcgen05.mma (M=128,
-// N=BN, K=16, fp32 accumulate) into one of two TMEM accumulators, so the MMAs
-// of tile i+1 run while warps 2-5 drain tile i. The epilogue reads TMEM with
-// tcgen05.ld (one output pixel per thread), adds the bias, applies ReLU,
-// rounds to fp16/bf16, stages 32 output channels at a time in shared memory
-// and writes them with TMA bulk-tensor stores into the NCHW/NCDHW output
-// (plain coalesced stores when the output rows are not 16-byte aligned).
+// N=NP, K=16, fp32 accumulate) into one of two TMEM accumulators, so the MMAs
+// of tile i+1 run while the epilogue drains tile i. The accumulator's TMEM
+// lanes are output channels and its columns pixels, so each of the eight
+// epilogue warps (two per lane quadrant, alternate 32-pixel chunks) reads 32
+// consecutive pixels of one channel per thread with tcgen05.ld, adds the
+// bias, applies ReLU, rounds to fp16/bf16 and writes 16-byte vectors
+// straight from registers into the NCHW/NCDHW output.
 //
 // Every wait on an mbarrier is bounded (SM cycle counter); on expiry the
 // kernel records an error word, lets its own in-flight copies and MMAs land,
@@ -51,16 +52,12 @@ cudaError_t read_and_clear_device_error(unsigned int *code) {
 namespace {
 
 constexpr int kEpiWarps = 8;                      // warps 2..9, two per TMEM lane quadrant
-constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kGroupThreads = 128;                // one epilogue group = 4 warps = 128 lanes
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 8;
 constexpr int kBlockK = 64;                       // channels per stage: one 128-B row
-constexpr uint32_t kAStageBytes = 128u * 128u;    // 128 pixel rows x 128 B
-constexpr int kEpiChunk = 32;                     // output channels per staged store
-constexpr uint32_t kStageOutBytes = 128u * kEpiChunk * 2u;   // 8 KB
-// Epilogue used when the output is 16-byte aligned: 2 = vector stores, 1 = TMA stores.
-constexpr int kEpiModeAligned = 2;
+constexpr int kTileOc = 128;                      // MMA M: output channels per tile
+constexpr uint32_t kWStageBytes = 128u * 128u;    // 128 channel rows x 128 B
+constexpr int kColChunk = 32;                     // accumulator columns per tcgen05.ld
 
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -108,13 +105,6 @@ __device__ __forceinline__ void raise_abort(volatile int *flag) {
     *flag = 1;
     atomicOr(&g_device_error, 1u);
 }
-__device__ __forceinline__ void epi_bar() {   // named barrier of all epilogue warps
-    asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-}
-__device__ __forceinline__ void group_bar(int grp) {   // barrier of one epilogue group
-    asm volatile("bar.sync %0, %1;" ::"r"(2 + grp), "n"(kGroupThreads) : "memory");
-}
-
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *tm, uint32_t bar,
                                             int c0, int c1, int c2, int c3, int c4) {
     asm volatile(
@@ -130,26 +120,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
-}
-__device__ __forceinline__ void tma_store_5d(const CUtensorMap *tm, uint32_t src, int c0, int c1,
-                                             int c2, int c3, int c4) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::
-            "l"(reinterpret_cast<uint64_t>(tm)),
-        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
@@ -229,14 +199,14 @@ struct TcArgs {
     void *y;
     int OC, OD, OH, OW;
     int k, pad, pad_d, stride;
-    int BW, BH, BN;
-    int tiles_w, tiles_h, n_tiles;
+    int BW, BH, NP;        // pixel tile: BH rows x BW columns; NP = MMA N >= BW*BH
+    int tiles_w, tiles_h, oc_tiles;
     int num_tiles;
     int cblocks;
     int ksteps;
     int stages;
     int relu;
-    int epi_mode;          // 0: direct element stores, 1: TMA tensor stores, 2: 16-byte stores
+    int vec_store;         // 16-byte stores of 8 pixels (aligned rows and tiles)
     uint32_t idesc;
     uint32_t tx_bytes;
     uint32_t tmem_cols;
@@ -246,41 +216,42 @@ struct TcArgs {
 struct TileCoord {
     int n, od, oh0, ow0, oc0;
 };
+// Tile t: output-channel block fastest (consecutive CTAs share the pixels,
+// the weights of a block are read by every CTA), then the pixel tiles.
 __device__ __forceinline__ TileCoord tile_coord(const TcArgs &a, int t) {
     TileCoord c;
-    const int nt = t % a.n_tiles;
-    t /= a.n_tiles;
+    const int ot = t % a.oc_tiles;
+    t /= a.oc_tiles;
     const int tw = t % a.tiles_w; t /= a.tiles_w;
     const int th = t % a.tiles_h; t /= a.tiles_h;
     c.od = t % a.OD;
     c.n = t / a.OD;
     c.ow0 = tw * a.BW;
     c.oh0 = th * a.BH;
-    c.oc0 = nt * a.BN;
+    c.oc0 = ot * kTileOc;
     return c;
 }
 
+// Accumulator orientation: TMEM lane = output channel, column = pixel of the
+// tile, so an epilogue thread owns consecutive pixels of one output channel,
+// which is how NCHW stores them.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
-igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmY, const TcArgs a) {
+igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t b_stage = (uint32_t)a.BN * 128u;
-    const uint32_t sA = base;
-    const uint32_t sB = sA + (uint32_t)a.stages * kAStageBytes;
-    const uint32_t sOut = sB + (uint32_t)a.stages * b_stage;          // 2 groups x 2 x 8 KB
-    const uint32_t sBias = sOut + 4u * kStageOutBytes;                // 256 floats
-    const uint32_t sBar = sBias + 1024u;
+    const uint32_t x_stage = (uint32_t)a.NP * 128u;
+    const uint32_t sW = base;
+    const uint32_t sX = sW + (uint32_t)a.stages * kWStageBytes;
+    const uint32_t sBar = sX + (uint32_t)a.stages * x_stage;
     const uint32_t full0 = sBar, empty0 = sBar + 8u * kMaxStages;
     const uint32_t tfull0 = sBar + 16u * kMaxStages, tempty0 = tfull0 + 16u;
     const uint32_t drain_bar = tempty0 + 16u;
     const uint32_t slot_addr = drain_bar + 8u;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem_raw + (slot_addr - raw));
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + (slot_addr + 4u - raw));
-    volatile int *epi_fail = reinterpret_cast<volatile int *>(smem_raw + (slot_addr + 8u - raw));
-    float *bias_s = reinterpret_cast<float *>(smem_raw + (sBias - raw));
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -295,13 +266,11 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
-        *epi_fail = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-        if (a.epi_mode == 1) prefetch_tmap(&tmY);
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
     }
     if (warp == 1) {
         tmem_alloc(slot_addr, a.tmem_cols);
@@ -334,9 +303,9 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         break;
                     }
                     mbar_arrive_expect_tx(fb, a.tx_bytes);
-                    tma_load_5d(sA + (uint32_t)s * kAStageBytes, &tmA, fb, cb * kBlockK, x0 + kx,
+                    tma_load_3d(sW + (uint32_t)s * kWStageBytes, &tmW, fb, cb * kBlockK, tc.oc0, tap);
+                    tma_load_5d(sX + (uint32_t)s * x_stage, &tmX, fb, cb * kBlockK, x0 + kx,
                                 y0 + ky, z0 + kz, tc.n);
-                    tma_load_3d(sB + (uint32_t)s * b_stage, &tmB, fb, cb * kBlockK, tc.oc0, tap);
                     ++issued;
                     if (++cb == a.cblocks) {
                         cb = 0;
@@ -361,8 +330,8 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
-            const uint64_t adesc0 = sw128_kmajor_desc(sA), bdesc0 = sw128_kmajor_desc(sB);
-            const uint32_t a_step = kAStageBytes >> 4, b_step = b_stage >> 4;
+            const uint64_t wdesc0 = sw128_kmajor_desc(sW), xdesc0 = sw128_kmajor_desc(sX);
+            const uint32_t w_step = kWStageBytes >> 4, x_step = x_stage >> 4;
             int s = 0;
             uint32_t ph = 0;
             int local = 0;
@@ -375,9 +344,8 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * a.BN);
-                uint64_t ad = adesc0, bd = bdesc0;
-                for (int k = 0; k < s; ++k) { ad += a_step; bd += b_step; }
+                const uint32_t d = tmem + (uint32_t)(acc * a.NP);
+                uint64_t wd = wdesc0 + (uint64_t)s * w_step, xd = xdesc0 + (uint64_t)s * x_step;
                 for (int it = 0; it < a.ksteps; ++it) {
                     if (!wait_bounded(full0 + 8u * s, ph, limit, abort_flag)) {
                         ok = false;
@@ -386,15 +354,15 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk)
-                        tc_mma(d, ad + 2u * kk, bd + 2u * kk, a.idesc, (it | kk) != 0);
+                        tc_mma(d, wd + 2u * kk, xd + 2u * kk, a.idesc, (it | kk) != 0);
                     tc_commit(empty0 + 8u * s);
-                    ad += a_step;
-                    bd += b_step;
+                    wd += w_step;
+                    xd += x_step;
                     if (++s == a.stages) {
                         s = 0;
                         ph ^= 1u;
-                        ad = adesc0;
-                        bd = bdesc0;
+                        wd = wdesc0;
+                        xd = xdesc0;
                     }
                 }
                 if (ok) tc_commit(tfull0 + 8u * acc);
@@ -408,22 +376,14 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // Two groups of four warps; warp w reads TMEM lane quadrant w % 4, and
-        // group g drains the 32-column chunks g, g+2, g+4, ...
+        // Warp w reads TMEM lane quadrant w % 4 (32 output channels); the two
+        // warps of a quadrant take alternate 32-pixel column chunks.
         const int q = warp & 3;
         const int grp = (warp - 2) / 4;
-        const int et = threadIdx.x - 64;      // 0..255
-        const int gt = et & (kGroupThreads - 1);
-        const int m = q * 32 + lane;          // accumulator row = tile pixel
-        const int r = m / a.BW, c = m - r * a.BW;
         const int MT = a.BW * a.BH;
-        const int64_t plane = (int64_t)a.OD * a.OH * a.OW;
-        T *out_g = reinterpret_cast<T *>(smem_raw + (sOut - raw)) +
-                   grp * 2 * (kStageOutBytes / sizeof(T));
-        const uint32_t sOut_g = sOut + (uint32_t)grp * 2u * kStageOutBytes;
-        const int nchunks = a.BN / kEpiChunk;
+        const int nchunks = (MT + kColChunk - 1) / kColChunk;
+        const int64_t plane = (int64_t)a.OH * a.OW;
         int local = 0;
-        int chunk_ctr = 0;
         for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++local) {
             const TileCoord tc = tile_coord(a, t);
             const int acc = local & 1;
@@ -431,78 +391,47 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             if (lane == 0)
                 ok = wait_bounded(tfull0 + 8u * acc, (uint32_t)(local >> 1) & 1u, limit, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok && lane == 0) *epi_fail = 1;
-            // One decision for all epilogue warps (they share named barriers);
-            // this barrier also orders the previous tile's bias reads.
-            epi_bar();
-            if (*epi_fail) {
-                if (et == 0) raise_abort(abort_flag);
+            if (!ok) {
+                if (lane == 0) raise_abort(abort_flag);
                 break;
             }
             tc_fence_after();
-            for (int j = et; j < a.BN; j += kEpiThreads) {
-                const int oc = tc.oc0 + j;
-                bias_s[j] = (a.b && oc < a.OC) ? __ldg(a.b + oc) : 0.0f;
-            }
-            epi_bar();
-            const int oh = tc.oh0 + r, ow = tc.ow0 + c;
-            const bool valid = m < MT && oh < a.OH && ow < a.OW;
-            T *yp = static_cast<T *>(a.y) +
-                    ((int64_t)tc.n * a.OC * a.OD + tc.od) * ((int64_t)a.OH * a.OW) +
-                    (int64_t)oh * a.OW + ow;
+            const int oc = tc.oc0 + q * 32 + lane;
+            const bool oc_ok = oc < a.OC;
+            const float bias = (a.b && oc_ok) ? __ldg(a.b + oc) : 0.0f;
+            T *yc = static_cast<T *>(a.y) +
+                    ((int64_t)tc.n * a.OC + (oc_ok ? oc : 0)) * a.OD * plane + (int64_t)tc.od * plane;
             for (int ch = grp; ch < nchunks; ch += 2) {
                 uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.BN + ch * kEpiChunk), v);
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.NP + ch * kColChunk), v);
                 tmem_ld_wait();
-                const float *bb = bias_s + ch * kEpiChunk;
-                if (a.epi_mode == 0) {
-                    if (valid) {
+                if (!oc_ok) continue;
+                const int p0 = ch * kColChunk;
+                if (a.vec_store) {
 #pragma unroll
-                        for (int j = 0; j < kEpiChunk; ++j) {
-                            const int oc = tc.oc0 + ch * kEpiChunk + j;
-                            if (oc < a.OC)
-                                yp[(int64_t)oc * plane] =
-                                    Storage<T>::from_float(epilogue(__uint_as_float(v[j]), bb[j], a.relu));
+                    for (int i8 = 0; i8 < kColChunk / 8; ++i8) {
+                        const int p = p0 + 8 * i8;
+                        const int r = a.BH == 1 ? 0 : p / a.BW;
+                        const int c = p - r * a.BW;
+                        if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW) {
+                            alignas(16) T h[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                h[e] = Storage<T>::from_float(
+                                    epilogue(__uint_as_float(v[8 * i8 + e]), bias, a.relu));
+                            *reinterpret_cast<uint4 *>(yc + (int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) =
+                                *reinterpret_cast<const uint4 *>(h);
                         }
                     }
                 } else {
-                    const int buf = chunk_ctr & 1;
-                    T *o = out_g + buf * (kStageOutBytes / sizeof(T));
-                    if (a.epi_mode == 1) {
-                        if (gt == 0) bulk_wait_read_1();   // the store that used `buf` has read it
-                        group_bar(grp);
-                    }
-                    if (m < MT) {
 #pragma unroll
-                        for (int j = 0; j < kEpiChunk; ++j)
-                            o[j * MT + m] = Storage<T>::from_float(epilogue(__uint_as_float(v[j]), bb[j], a.relu));
+                    for (int e = 0; e < kColChunk; ++e) {
+                        const int p = p0 + e;
+                        const int r = p / a.BW, c = p - r * a.BW;
+                        if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
+                            yc[(int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c] =
+                                Storage<T>::from_float(epilogue(__uint_as_float(v[e]), bias, a.relu));
                     }
-                    if (a.epi_mode == 1) {
-                        fence_proxy_async_smem();
-                        group_bar(grp);
-                        if (gt == 0) {
-                            tma_store_5d(&tmY, sOut_g + buf * kStageOutBytes, tc.ow0, tc.oh0, tc.od,
-                                         tc.oc0 + ch * kEpiChunk, tc.n);
-                            bulk_commit();
-                        }
-                    } else {
-                        // 16-byte stores of 8 consecutive pixels of one channel.
-                        group_bar(grp);
-                        const int vpr = MT / 8;            // vectors per channel row
-                        for (int vi = gt; vi < kEpiChunk * vpr; vi += kGroupThreads) {
-                            const int j = vi / vpr, pv = (vi - j * vpr) * 8;
-                            const int oc = tc.oc0 + ch * kEpiChunk + j;
-                            const int rr = pv / a.BW, cc = pv - rr * a.BW;
-                            if (oc < a.OC && tc.oh0 + rr < a.OH && tc.ow0 + cc < a.OW) {
-                                T *dst = static_cast<T *>(a.y) +
-                                         (((int64_t)tc.n * a.OC + oc) * a.OD + tc.od) * ((int64_t)a.OH * a.OW) +
-                                         (int64_t)(tc.oh0 + rr) * a.OW + tc.ow0 + cc;
-                                *reinterpret_cast<uint4 *>(dst) =
-                                    *reinterpret_cast<const uint4 *>(o + j * MT + pv);
-                            }
-                        }
-                    }
-                    ++chunk_ctr;
                 }
             }
             // All reads of this accumulator by this warp are done: hand it back.
@@ -510,7 +439,6 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
         }
-        if (a.epi_mode == 1 && gt == 0) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -618,42 +546,40 @@ cudaError_t dev_info(DevInfo *out) {
     return cudaSuccess;
 }
 
-// Output-tile geometry: BH rows x BW columns of one (n, od) plane, BW*BH <= 128,
-// boxes of at most 256 traversed elements per axis; BN a multiple of 32.
+// Pixel-tile geometry: BH rows x BW columns of one (n, od) plane, at most 256
+// pixels (MMA N, rounded up to a multiple of 16), boxes of at most 256
+// traversed elements per axis; whole output rows when they fit.
 struct TileGeom {
-    int BW, BH, BN, stages;
+    int BW, BH, NP, stages;
 };
 
 TileGeom choose_geom(const Problem &p) {
     TileGeom g{};
-    const int bw_max = 256 / p.stride < 128 ? 256 / p.stride : 128;
-    if (p.OW >= bw_max) {
+    const int bw_max = 256 / p.stride;
+    if (p.OW > bw_max) {
         const int tiles = (p.OW + bw_max - 1) / bw_max;
         g.BW = (p.OW + tiles - 1) / tiles;
-        // prefer 16-byte aligned column tiles (TMA-store epilogue)
-        const int bw8 = (g.BW + 7) / 8 * 8;
+        const int bw8 = (g.BW + 7) / 8 * 8;          // 16-byte aligned column tiles
         if (bw8 <= bw_max && (p.OW + bw8 - 1) / bw8 == tiles) g.BW = bw8;
         g.BH = 1;
     } else {
         g.BW = p.OW;
-        int bh = 128 / p.OW;
+        int bh = 256 / p.OW;
         const int bh_max = 256 / p.stride;
         if (bh > bh_max) bh = bh_max;
         if (bh > p.OH) bh = p.OH;
         g.BH = bh < 1 ? 1 : bh;
     }
-    int bn = (p.OC + 31) / 32 * 32;
-    g.BN = bn > 256 ? 256 : bn;
-    const int stage_bytes = (int)kAStageBytes + g.BN * 128;
-    const int fixed = 1024 + 4 * (int)kStageOutBytes + 1024 + 256;
+    g.NP = (g.BW * g.BH + 15) / 16 * 16;
+    const int stage_bytes = (int)kWStageBytes + g.NP * 128;
+    const int fixed = 1024 + 256;
     int st = (227 * 1024 - fixed) / stage_bytes;
     g.stages = st > kMaxStages ? kMaxStages : st;
     return g;
 }
 
 size_t smem_bytes(const TileGeom &g) {
-    return 1024 + (size_t)g.stages * (kAStageBytes + (size_t)g.BN * 128) + 4 * kStageOutBytes +
-           1024 + 256;
+    return 1024 + (size_t)g.stages * (kWStageBytes + (size_t)g.NP * 128) + 256;
 }
 
 uint32_t tmem_cols_for(int cols) {
@@ -675,8 +601,10 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     const CUtensorMapDataType dt =
         p.dtype == GBCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
-    alignas(64) CUtensorMap tmA, tmB, tmY;
+    alignas(64) CUtensorMap tmX, tmW;
     {
+        // Channels-last input as {Cp, W, H, D, N}; a box is 64 channels of one
+        // tile's (shifted) pixels; the conv stride is the element stride.
         const cuuint64_t dims[5] = {(cuuint64_t)Cp, (cuuint64_t)p.W, (cuuint64_t)p.H,
                                     (cuuint64_t)p.D, (cuuint64_t)p.N};
         const cuuint64_t strides[4] = {(cuuint64_t)Cp * 2, (cuuint64_t)Cp * 2 * p.W,
@@ -685,41 +613,23 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
         const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)(g.BW * p.stride),
                                    (cuuint32_t)(g.BH * p.stride), 1, 1};
         const cuuint32_t es[5] = {1, (cuuint32_t)p.stride, (cuuint32_t)p.stride, 1, 1};
-        if (encode(&tmA, dt, 5, const_cast<void *>(xc), dims, strides, box, es,
+        if (encode(&tmX, dt, 5, const_cast<void *>(xc), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     {
+        // Packed weights {Cp, OC, taps}; a box is 64 channels x 128 outputs.
         const cuuint64_t dims[3] = {(cuuint64_t)Cp, (cuuint64_t)p.OC, (cuuint64_t)p.taps};
         const cuuint64_t strides[2] = {(cuuint64_t)Cp * 2, (cuuint64_t)Cp * 2 * p.OC};
-        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)g.BN, 1};
+        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)kTileOc, 1};
         const cuuint32_t es[3] = {1, 1, 1};
-        if (encode(&tmB, dt, 3, const_cast<void *>(wp), dims, strides, box, es,
+        if (encode(&tmW, dt, 3, const_cast<void *>(wp), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-    }
-    // Epilogue store mode. 16-byte vector stores (mode 2) and TMA tensor
-    // stores (mode 1) need 16-byte output rows, 16-byte column tiles and a
-    // 16-byte aligned base; otherwise elements are stored one by one (mode 0).
-    const bool aligned16 = (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
-    int epi_mode = aligned16 ? kEpiModeAligned : 0;
-    memset(&tmY, 0, sizeof(tmY));
-    if (epi_mode == 1) {
-        const cuuint64_t dims[5] = {(cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.OD,
-                                    (cuuint64_t)p.OC, (cuuint64_t)p.N};
-        const cuuint64_t strides[4] = {(cuuint64_t)p.OW * 2, (cuuint64_t)p.OW * 2 * p.OH,
-                                       (cuuint64_t)p.OW * 2 * p.OH * p.OD,
-                                       (cuuint64_t)p.OW * 2 * p.OH * p.OD * p.OC};
-        const cuuint32_t box[5] = {(cuuint32_t)g.BW, (cuuint32_t)g.BH, 1, (cuuint32_t)kEpiChunk, 1};
-        const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-        if (encode(&tmY, dt, 5, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            epi_mode = 2;
     }
 
     TcArgs a{};
@@ -727,20 +637,20 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.y = y;
     a.OC = p.OC; a.OD = p.OD; a.OH = p.OH; a.OW = p.OW;
     a.k = p.k; a.pad = p.pad; a.pad_d = p.pad_d; a.stride = p.stride;
-    a.BW = g.BW; a.BH = g.BH; a.BN = g.BN;
+    a.BW = g.BW; a.BH = g.BH; a.NP = g.NP;
     a.tiles_w = (p.OW + g.BW - 1) / g.BW;
     a.tiles_h = (p.OH + g.BH - 1) / g.BH;
-    a.n_tiles = (p.OC + g.BN - 1) / g.BN;
-    const int64_t num_tiles = (int64_t)p.N * p.OD * a.tiles_h * a.tiles_w * a.n_tiles;
+    a.oc_tiles = (p.OC + kTileOc - 1) / kTileOc;
+    const int64_t num_tiles = (int64_t)p.N * p.OD * a.tiles_h * a.tiles_w * a.oc_tiles;
     a.num_tiles = (int)num_tiles;
     a.cblocks = (Cp + kBlockK - 1) / kBlockK;
     a.ksteps = p.taps * a.cblocks;
     a.stages = g.stages;
     a.relu = p.act == GBCONV_ACT_RELU;
-    a.epi_mode = epi_mode;
-    a.idesc = make_idesc(128, g.BN, p.dtype == GBCONV_BF16);
-    a.tx_bytes = kAStageBytes / 128u * (uint32_t)(g.BW * g.BH) + (uint32_t)g.BN * 128u;
-    a.tmem_cols = tmem_cols_for(2 * g.BN);
+    a.vec_store = (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
+    a.idesc = make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
+    a.tx_bytes = kWStageBytes + 128u * (uint32_t)(g.BW * g.BH);
+    a.tmem_cols = tmem_cols_for(2 * g.NP);
     const double cyc = (double)wait_limit_ns() * (double)info.clock_khz * 1e-6;
     a.wait_limit_cycles = cyc > 9.0e18 ? (long long)9e18 : (long long)cyc;
 
@@ -755,7 +665,7 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
         attr_done.fetch_or(1ull << (dev & 63));
     }
     const int grid = num_tiles < info.sms ? (int)num_tiles : info.sms;
-    kern<<<grid, kThreads, smem, s>>>(tmA, tmB, tmY, a);
+    kern<<<grid, kThreads, smem, s>>>(tmX, tmW, a);
     return cudaGetLastError();
 }
 
@@ -789,7 +699,7 @@ bool tc_supported(const Problem &p) {
     if (p.dtype == GBCONV_F32) return false;
     const TileGeom g = choose_geom(p);
     const int64_t mtiles = (int64_t)p.N * p.OD * ((p.OH + g.BH - 1) / g.BH) *
-                           ((p.OW + g.BW - 1) / g.BW) * ((p.OC + g.BN - 1) / g.BN);
+                           ((p.OW + g.BW - 1) / g.BW) * ((p.OC + kTileOc - 1) / kTileOc);
     return g.BW * p.stride <= 256 && g.BH * p.stride <= 256 && mtiles < 0x7FFFFFFF &&
            g.stages >= 2 && p.N <= 65535;
 }
