@@ -283,18 +283,17 @@ __global__ void __launch_bounds__(WNT, kWideMinBlocks) igemm_ffma2_kernel(const 
     }
 }
 
-// wp[(tap * C + c) * OCp + oc] = w[(oc * C + c) * taps + tap], zero-padded in oc.
+// wp[(tap * C + c) * OCp + oc] = w[(oc * C + c) * taps + tap], zero-padded in
+// oc. One CTA per (tap, c) row of the output; threads walk the channels.
 template <typename T>
 __global__ void pack_ffma_kernel(const T *__restrict__ w, T *__restrict__ wp,
                                  int OC, int C, int taps, int OCp) {
-    const int64_t total = (int64_t)taps * C * OCp;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int oc = (int)(e % OCp);
-        const int64_t kk = e / OCp;
-        const int c = (int)(kk % C), tap = (int)(kk / C);
-        wp[e] = oc < OC ? w[((int64_t)oc * C + c) * taps + tap] : T(0.0f);
-    }
+    const int row = blockIdx.x;                 // tap * C + c
+    const int tap = row / C, c = row - tap * C;
+    const T *src = w + (int64_t)c * taps + tap;
+    T *dst = wp + (int64_t)row * OCp;
+    for (int oc = threadIdx.x; oc < OCp; oc += blockDim.x)
+        dst[oc] = oc < OC ? src[(int64_t)oc * C * taps] : T(0.0f);
 }
 
 template <typename T>
@@ -315,10 +314,9 @@ cudaError_t launch_ffma_typed(const FfmaArgs &a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_pack_typed(const Problem &p, const void *w, void *wp, cudaStream_t s) {
-    const int64_t total = (int64_t)p.taps * p.C * ffma_ocpad(p.OC);
-    const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-    pack_ffma_kernel<T><<<blocks, 256, 0, s>>>(static_cast<const T *>(w), static_cast<T *>(wp),
-                                               p.OC, p.C, p.taps, ffma_ocpad(p.OC));
+    const int OCp = ffma_ocpad(p.OC);
+    pack_ffma_kernel<T><<<p.taps * p.C, OCp < 256 ? OCp : 256, 0, s>>>(
+        static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.C, p.taps, OCp);
     return cudaGetLastError();
 }
 

@@ -35,8 +35,11 @@
 #include "internal.h"
 
 namespace gbconv {
-
 __device__ unsigned int g_device_error;   // bit 0: a bounded wait ran out
+}
+#include "tc_ptx.cuh"
+
+namespace gbconv {
 static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
@@ -51,6 +54,8 @@ cudaError_t read_and_clear_device_error(unsigned int *code) {
 
 namespace {
 
+using namespace tc;
+
 constexpr int kEpiWarps = 8;                      // warps 2..9, two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 8;
@@ -58,141 +63,6 @@ constexpr int kBlockK = 64;                       // channels per stage: one 128
 constexpr int kTileOc = 128;                      // MMA M: output channels per tile
 constexpr uint32_t kWStageBytes = 128u * 128u;    // 128 channel rows x 128 B
 constexpr int kColChunk = 32;                     // accumulator columns per tcgen05.ld
-
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Wait until the phase with the given parity has completed, for at most
-// `limit` SM cycles; gives up early when another role raised the abort flag.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, long long limit,
-                                             const volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (abort_flag && *abort_flag) return false;
-        if (clock64() - t0 > limit) return false;
-    }
-}
-__device__ __forceinline__ void raise_abort(volatile int *flag) {
-    *flag = 1;
-    atomicOr(&g_device_error, 1u);
-}
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *tm, uint32_t bar,
-                                            int c0, int c1, int c2, int c3, int c4) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, uint32_t bar,
-                                            int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
-// layout: rows of 64 16-bit elements (128 B), 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);   // start address
-    d |= (uint64_t)1u << 16;                    // leading byte offset (unused here)
-    d |= (uint64_t)(1024u >> 4) << 32;          // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1u << 46;                    // descriptor version for tcgen05
-    d |= (uint64_t)2u << 61;                    // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, A/B fp16 or bf16,
-// both K-major, shape M x N.
-constexpr uint32_t make_idesc(int M, int N, bool bf16) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
 
 struct TcArgs {
     const float *b;
@@ -450,59 +320,76 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 }
 
 // x [N][C][S] -> xc [N][S][Cp], zero in channels C..Cp-1 (S = D*H*W).
-// 64 channels x 64 positions per CTA; 16-byte global loads and stores when
-// x rows are 16-byte aligned (VEC), element loads otherwise.
+// A CTA moves 64 channels x 128 positions (16 KB) through shared memory:
+// loads are 16-byte vectors along a channel's positions (16 lanes = 256
+// contiguous bytes), stores 16-byte vectors of 8 channels (8 lanes = one
+// position's 128 contiguous bytes). The shared tile keeps a channel's row of
+// positions in 16-byte chunks whose index is XOR-ed with (channel / 8), so
+// the column reads of the store phase hit 16 different banks per warp.
+constexpr int kClC = 64, kClS = 128;
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(256)
 to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S) {
-    __shared__ __align__(16) T tile[64][72];
-    const int64_t s0 = (int64_t)blockIdx.x * 64;
-    const int c0 = blockIdx.y * 64;
+    __shared__ __align__(16) T tile[kClC][kClS];
+    const int64_t s0 = (int64_t)blockIdx.x * kClS;
+    const int c0 = blockIdx.y * kClC;
     const int n = blockIdx.z;
     const T *xn = x + (int64_t)n * C * S;
     T *xcn = xc + (int64_t)n * S * Cp;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kClC * kClS / 8 / 256; ++i) {
         const int v = threadIdx.x + 256 * i;
-        const int cl = v / 8, p = (v % 8) * 8;
+        const int cl = v / 16, p8 = v % 16;
         const int cc = c0 + cl;
-        const int64_t s = s0 + p;
+        const int64_t s = s0 + p8 * 8;
+        T *dst = &tile[cl][(p8 ^ ((cl >> 3) & 7)) * 8];
         if (VEC && cc < C && s + 8 <= S) {
-            *reinterpret_cast<uint4 *>(&tile[cl][p]) =
-                __ldg(reinterpret_cast<const uint4 *>(xn + (int64_t)cc * S + s));
+            *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(xn + (int64_t)cc * S + s));
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                tile[cl][p + j] = (cc < C && s + j < S) ? xn[(int64_t)cc * S + s + j] : T(0.0f);
+                dst[j] = (cc < C && s + j < S) ? xn[(int64_t)cc * S + s + j] : T(0.0f);
         }
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kClC * kClS / 8 / 256; ++i) {
         const int v = threadIdx.x + 256 * i;
-        const int pl = v % 64, cch = v / 64;          // lanes walk positions
+        const int cch = v % 8, pos = v / 8;
         const int cc = c0 + cch * 8;
-        const int64_t s = s0 + pl;
+        const int64_t s = s0 + pos;
         if (s < S && cc < Cp) {
+            const int col = (((pos >> 3) ^ cch) << 3) | (pos & 7);
             alignas(16) T vals[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) vals[j] = tile[cch * 8 + j][pl];
+            for (int j = 0; j < 8; ++j) vals[j] = tile[cch * 8 + j][col];
             *reinterpret_cast<uint4 *>(xcn + s * Cp + cc) = *reinterpret_cast<const uint4 *>(vals);
         }
     }
 }
 
-// wp[tap][oc][cp] = w[oc][c][tap] for c < C, zero for C <= cp < Cp.
+// wp[tap][oc][cp] = w[oc][c][tap] for c < C, zero for C <= cp < Cp. A CTA
+// handles one output channel, 64 channels and up to 32 taps: it reads
+// w[oc][c][tap0 ..] runs (contiguous along taps) into shared memory and
+// writes each tap's 64 channels as one 128-byte run of wp.
+constexpr int kPkC = 64, kPkT = 32;
 template <typename T>
-__global__ void pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C,
-                               int Cp, int taps) {
-    const int64_t total = (int64_t)taps * OC * Cp;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int cp = (int)(e % Cp);
-        const int64_t r = e / Cp;
-        const int oc = (int)(r % OC), tap = (int)(r / OC);
-        wp[e] = cp < C ? w[((int64_t)oc * C + cp) * taps + tap] : T(0.0f);
+__global__ void __launch_bounds__(256)
+pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp, int taps) {
+    __shared__ T tile[kPkC][kPkT + 1];
+    const int oc = blockIdx.x;
+    const int c0 = blockIdx.y * kPkC, t0 = blockIdx.z * kPkT;
+    const T *src = w + (int64_t)oc * C * taps;
+    for (int e = threadIdx.x; e < kPkC * kPkT; e += blockDim.x) {
+        const int cl = e / kPkT, tl = e % kPkT;
+        const int c = c0 + cl, t = t0 + tl;
+        tile[cl][tl] = (c < C && t < taps) ? src[(int64_t)c * taps + t] : T(0.0f);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kPkC * kPkT; e += blockDim.x) {
+        const int tl = e / kPkC, cl = e % kPkC;
+        const int cp = c0 + cl, t = t0 + tl;
+        if (cp < Cp && t < taps) wp[((int64_t)t * OC + oc) * Cp + cp] = tile[cl][tl];
     }
 }
 
@@ -650,7 +537,11 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.vec_store = (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
     a.idesc = make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
     a.tx_bytes = kWStageBytes + 128u * (uint32_t)(g.BW * g.BH);
-    a.tmem_cols = tmem_cols_for(2 * g.NP);
+    {
+        // Accumulator 1's last 32-column epilogue read may run past 2 * NP.
+        const int last = g.NP + (g.BW * g.BH + kColChunk - 1) / kColChunk * kColChunk;
+        a.tmem_cols = tmem_cols_for(last > 2 * g.NP ? last : 2 * g.NP);
+    }
     const double cyc = (double)wait_limit_ns() * (double)info.clock_khz * 1e-6;
     a.wait_limit_cycles = cyc > 9.0e18 ? (long long)9e18 : (long long)cyc;
 
@@ -673,7 +564,7 @@ template <typename T>
 cudaError_t launch_cl_typed(const Problem &p, const void *x, void *xc, cudaStream_t s) {
     const int Cp = tc_cpad(p.C);
     const int64_t S = p.in_vol;
-    dim3 grid((unsigned)((S + 63) / 64), (unsigned)((Cp + 63) / 64), (unsigned)p.N);
+    dim3 grid((unsigned)((S + kClS - 1) / kClS), (unsigned)((Cp + kClC - 1) / kClC), (unsigned)p.N);
     const bool vec = (S % 8 == 0) && ((uintptr_t)x % 16 == 0);
     if (vec)
         to_channels_last_kernel<T, true><<<grid, 256, 0, s>>>(static_cast<const T *>(x),
@@ -686,10 +577,10 @@ cudaError_t launch_cl_typed(const Problem &p, const void *x, void *xc, cudaStrea
 
 template <typename T>
 cudaError_t launch_pack_tc_typed(const Problem &p, const void *w, void *wp, cudaStream_t s) {
-    const int64_t total = (int64_t)p.taps * p.OC * tc_cpad(p.C);
-    const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-    pack_tc_kernel<T><<<blocks, 256, 0, s>>>(static_cast<const T *>(w), static_cast<T *>(wp), p.OC,
-                                             p.C, tc_cpad(p.C), p.taps);
+    const int Cp = tc_cpad(p.C);
+    dim3 grid((unsigned)p.OC, (unsigned)((Cp + kPkC - 1) / kPkC), (unsigned)((p.taps + kPkT - 1) / kPkT));
+    pack_tc_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.C,
+                                           Cp, p.taps);
     return cudaGetLastError();
 }
 

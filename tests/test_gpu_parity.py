@@ -100,6 +100,20 @@ SWEEP = [
     (A_TC, _L(dtype="f16", C=16, D=5, H=8, W=40, OC=32, ndim=3)),
     (A_TC, _L(dtype="f16", C=32, D=1, H=10, W=12, OC=16, ndim=3)),
     (A_TC, _L(dtype="bf16", C=8, D=6, H=9, W=10, OC=24, ndim=3, stride=2)),
+    # tensor-core implicit GEMM read from NCHW in place (stride 1, W % 8 == 0):
+    # several rows per tile, one row per tile, column tiles with a ragged
+    # tail, partial channel blocks, OC tails, k 1/3/5/7, pad 0..3, 3D
+    (A_TC, _L(dtype="f16", N=2, C=72, H=5, W=152, OC=40, relu=True)),
+    (A_TC, _L(dtype="f16", C=136, H=7, W=32, OC=300, bias=False)),
+    (A_TC, _L(dtype="f16", C=32, H=17, W=64, OC=48, k=5, pad=2)),
+    (A_TC, _L(dtype="f16", C=16, H=12, W=16, OC=24, k=1, pad=0)),
+    (A_TC, _L(dtype="f16", C=8, H=3, W=520, OC=16)),
+    (A_TC, _L(dtype="f16", C=64, H=4, W=256, OC=130, pad=0)),
+    (A_TC, _L(dtype="f16", C=3, H=10, W=8, OC=16, pad=2)),
+    (A_TC, _L(dtype="f16", C=40, H=9, W=48, OC=20, k=7, pad=3, relu=True)),
+    (A_TC, _L(dtype="bf16", C=64, H=9, W=72, OC=128, relu=True)),
+    (A_TC, _L(dtype="bf16", C=24, D=3, H=6, W=24, OC=40, ndim=3)),
+    (A_TC, _L(dtype="f16", N=3, C=200, D=2, H=5, W=240, OC=64, ndim=3)),
 ]
 
 
