@@ -23,7 +23,7 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 F32, F16, BF16 = 0, 1, 2
 ACT_NONE, ACT_RELU = 0, 1
 W_OIHW, W_PACKED = 0, 1
-ALGO_AUTO, ALGO_DIRECT, ALGO_IGEMM_FFMA, ALGO_IGEMM_TC = 0, 1, 2, 3
+ALGO_AUTO, ALGO_DIRECT, ALGO_IGEMM_FFMA, ALGO_IGEMM_TC, ALGO_DIRECT_TC = 0, 1, 2, 3, 4
 DTYPES = {"f32": F32, "f16": F16, "bf16": BF16}
 SYMBOLS = ["gbconv_conv2d_fwd", "gbconv_conv3d_fwd", "gbconv_output_shape",
            "gbconv_workspace_size", "gbconv_weight_packed_size",

@@ -28,7 +28,7 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (!in_range(d->dtype, GBCONV_F32, GBCONV_BF16)) return GBCONV_ERR_DTYPE;
     if (!in_range(d->act, GBCONV_ACT_NONE, GBCONV_ACT_RELU)) return GBCONV_ERR_ACT;
     if (!in_range(d->w_layout, GBCONV_W_OIHW, GBCONV_W_PACKED)) return GBCONV_ERR_LAYOUT;
-    if (!in_range(d->algo, GBCONV_ALGO_AUTO, GBCONV_ALGO_IGEMM_TC)) return GBCONV_ERR_ALGO;
+    if (!in_range(d->algo, GBCONV_ALGO_AUTO, GBCONV_ALGO_DIRECT_TC)) return GBCONV_ERR_ALGO;
     const int dims[] = {d->N, d->C, d->D, d->H, d->W, d->OC};
     for (int v : dims)
         if (!in_range(v, 1, GBCONV_MAX_DIM)) return GBCONV_ERR_SHAPE;
@@ -65,7 +65,11 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     // 16-bit storage, exact fp32 FMA on CUDA cores for fp32.
     int algo = d->algo;
     if (algo == GBCONV_ALGO_AUTO) {
-        if ((int64_t)q.C * q.taps <= 64 && direct_supported(q))
+        // fp32 3x3 stems of 48+ output channels: the tensor-core stem (its
+        // cost does not grow with OC up to 128; measured faster from 64).
+        if (stem_tc_supported(q) && q.OC >= 48)
+            algo = GBCONV_ALGO_DIRECT_TC;
+        else if ((int64_t)q.C * q.taps <= 64 && direct_supported(q))
             algo = GBCONV_ALGO_DIRECT;
         else if (q.dtype != GBCONV_F32 && tc_supported(q))
             algo = GBCONV_ALGO_IGEMM_TC;
@@ -76,6 +80,7 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (algo == GBCONV_ALGO_DIRECT && !direct_supported(q)) return GBCONV_ERR_ALGO;
     if (algo == GBCONV_ALGO_IGEMM_TC && (q.dtype == GBCONV_F32 || !tc_supported(q)))
         return GBCONV_ERR_ALGO;
+    if (algo == GBCONV_ALGO_DIRECT_TC && !stem_tc_supported(q)) return GBCONV_ERR_ALGO;
     *p = q;
     return GBCONV_OK;
 }
@@ -129,6 +134,10 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
         // The direct kernel reads OIHW; its packed form is an OIHW copy.
         e = launch_direct(p, x, w, b, y, s);
         break;
+    case GBCONV_ALGO_DIRECT_TC:
+        // Reads OIHW as well (the tensor-core tiles are built in the kernel).
+        e = launch_stem_tc(p, x, w, b, y, s);
+        break;
     case GBCONV_ALGO_IGEMM_FFMA: {
         const void *wp = w;
         if (p.w_layout == GBCONV_W_OIHW) {
@@ -168,6 +177,7 @@ gbconv_status make_problem(const gbconv_desc *d, int ndim, Problem *p) {
 size_t packed_weight_bytes(const Problem &p) {
     switch (p.algo) {
     case GBCONV_ALGO_DIRECT:
+    case GBCONV_ALGO_DIRECT_TC:
         return (size_t)p.w_elems * p.elt;
     case GBCONV_ALGO_IGEMM_FFMA:
         return (size_t)p.taps * p.C * ffma_ocpad(p.OC) * p.elt;
@@ -185,7 +195,7 @@ Workspace workspace_layout(const Problem &p) {
         ws.x_bytes = (size_t)p.N * p.in_vol * tc_cpad(p.C) * p.elt;
         off = align256(off + ws.x_bytes);
     }
-    if (p.w_layout == GBCONV_W_OIHW && p.algo != GBCONV_ALGO_DIRECT) {
+    if (p.w_layout == GBCONV_W_OIHW && p.algo != GBCONV_ALGO_DIRECT && p.algo != GBCONV_ALGO_DIRECT_TC) {
         ws.w_off = off;
         ws.w_bytes = packed_weight_bytes(p);
         off = align256(off + ws.w_bytes);
@@ -257,6 +267,7 @@ gbconv_status gbconv_weight_pack(const gbconv_desc *desc, int ndim,
     cudaError_t e;
     switch (p.algo) {
     case GBCONV_ALGO_DIRECT:
+    case GBCONV_ALGO_DIRECT_TC:
         e = cudaMemcpyAsync(w_packed, w_oihw, (size_t)p.w_elems * p.elt,
                             cudaMemcpyDeviceToDevice, stream);
         break;
@@ -327,6 +338,7 @@ const char *gbconv_algo_name(int algo) {
     case GBCONV_ALGO_DIRECT: return "direct";
     case GBCONV_ALGO_IGEMM_FFMA: return "igemm_ffma";
     case GBCONV_ALGO_IGEMM_TC: return "igemm_tc";
+    case GBCONV_ALGO_DIRECT_TC: return "direct_tc";
     }
     return "unknown";
 }

@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "dev_common.cuh"
@@ -560,6 +561,8 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     return cudaGetLastError();
 }
 
+#include "stem_tf32.cuh"
+
 template <typename T>
 cudaError_t launch_cl_typed(const Problem &p, const void *x, void *xc, cudaStream_t s) {
     const int Cp = tc_cpad(p.C);
@@ -599,6 +602,23 @@ cudaError_t launch_igemm_tc(const Problem &p, const void *xc, const void *wp, co
                             void *y, cudaStream_t s) {
     if (p.dtype == GBCONV_BF16) return launch_tc_typed<__nv_bfloat16>(p, xc, wp, b, y, s);
     return launch_tc_typed<__half>(p, xc, wp, b, y, s);
+}
+
+bool stem_tc_supported(const Problem &p) {
+    return p.ndim == 2 && p.dtype == GBCONV_F32 && p.k == 3 && p.C <= 3 &&
+           (int64_t)p.N * p.OH * ((p.OW + 31) / 32) < (1ll << 33) &&
+           p.OC <= kStemMaxOC;
+}
+
+cudaError_t launch_stem_tc(const Problem &p, const void *x, const void *w, const float *b, void *y,
+                           cudaStream_t s) {
+    const float *xf = static_cast<const float *>(x), *wf = static_cast<const float *>(w);
+    float *yf = static_cast<float *>(y);
+    switch (p.C) {
+    case 1: return launch_stem_tf32_c<1>(p, xf, wf, b, yf, s);
+    case 2: return launch_stem_tf32_c<2>(p, xf, wf, b, yf, s);
+    default: return launch_stem_tf32_c<3>(p, xf, wf, b, yf, s);
+    }
 }
 
 cudaError_t launch_to_channels_last(const Problem &p, const void *x, void *xc, cudaStream_t s) {

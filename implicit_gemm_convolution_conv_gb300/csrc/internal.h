@@ -48,6 +48,7 @@ Workspace workspace_layout(const Problem &p);
 bool direct_supported(const Problem &p);
 bool stem_supported(const Problem &p);   // few-channel 3x3 direct kernel
 bool tc_supported(const Problem &p);
+bool stem_tc_supported(const Problem &p);   // fp32, 2D, k = 3, C <= 3: tensor cores, 3 TF32 products
 
 // Kernel launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_direct(const Problem &p, const void *x, const void *w_oihw,
@@ -63,6 +64,8 @@ cudaError_t launch_pack_tc(const Problem &p, const void *w_oihw,
                            void *w_packed, cudaStream_t s);
 cudaError_t launch_to_channels_last(const Problem &p, const void *x,
                                     void *x_cl, cudaStream_t s);
+cudaError_t launch_stem_tc(const Problem &p, const void *x, const void *w_oihw,
+                           const float *b, void *y, cudaStream_t s);
 // Returns cudaErrorInvalidValue when the tensor maps cannot be encoded.
 cudaError_t launch_igemm_tc(const Problem &p, const void *x_cl,
                             const void *w_packed, const float *b, void *y,

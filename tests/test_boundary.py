@@ -81,7 +81,7 @@ BAD = [
     (dict(N=4096, C=4096, H=4096, W=4096), gb.ERR_SHAPE),
     (dict(dtype=3), gb.ERR_DTYPE), (dict(dtype=-1), gb.ERR_DTYPE),
     (dict(act=2), gb.ERR_ACT), (dict(act=-7), gb.ERR_ACT),
-    (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=4), gb.ERR_ALGO),
+    (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, C=4), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, OC=129), gb.ERR_ALGO),
     (dict(reserved=1), gb.ERR_RESERVED),
     (dict(algo=gb.ALGO_IGEMM_TC), gb.ERR_ALGO),     # tensor cores need 16-bit
     (dict(C=64, algo=gb.ALGO_DIRECT, k=15, pad=7, H=64, W=64, OC=32),
@@ -161,6 +161,18 @@ def test_shapes_and_algorithm_of_the_five_layers(idx):
     assert algo == expect, gb.algo_name(algo)
 
 
+def test_auto_picks_tensor_core_stem_for_wide_fp32_stems():
+    """fp32 3x3 stems with 48+ output channels go to the tensor-core stem;
+    narrower ones, other dtypes and C > 3 do not."""
+    pick = lambda **kw: gb.select_algo(_desc(**kw), 2)[1]
+    assert pick(C=3, OC=64, H=640, W=640, k=3, pad=1, stride=2) == gb.ALGO_DIRECT_TC
+    assert pick(C=3, OC=128, H=64, W=64, k=3, pad=1, stride=1) == gb.ALGO_DIRECT_TC
+    assert pick(C=3, OC=32, H=640, W=640, k=3, pad=1, stride=2) == gb.ALGO_DIRECT
+    assert pick(C=4, OC=64, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
+    assert pick(C=3, OC=160, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
+    assert pick(C=3, OC=64, H=64, W=64, k=3, pad=1, stride=1, dtype=gb.F16) != gb.ALGO_DIRECT_TC
+
+
 def test_conv3d_shapes():
     d = gb.make_desc(1, 4, 6, 7, 2, k=3, pad=1, stride=2, D=5)
     assert gb.output_shape(d, 3) == (gb.OK, (3, 3, 4))
@@ -173,7 +185,7 @@ def test_status_and_algo_names():
     for s in range(0, 15):
         assert gb.status_string(s) and gb.status_string(s) != "unknown status"
     assert gb.status_string(99) == "unknown status"
-    assert [gb.algo_name(a) for a in range(4)] == [
-        "auto", "direct", "igemm_ffma", "igemm_tc"]
+    assert [gb.algo_name(a) for a in range(5)] == [
+        "auto", "direct", "igemm_ffma", "igemm_tc", "direct_tc"]
     assert gb.set_wait_limit_ns(0) == gb.ERR_SHAPE
     assert gb.set_wait_limit_ns(2_000_000_000) == gb.OK

@@ -22,6 +22,7 @@ from gpu_helpers import assert_close, device_inputs, reference, run
 pytestmark = pytest.mark.gpu
 
 A_DIRECT, A_FFMA, A_TC = gb.ALGO_DIRECT, gb.ALGO_IGEMM_FFMA, gb.ALGO_IGEMM_TC
+A_DTC = gb.ALGO_DIRECT_TC
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,6 +41,16 @@ def test_layer_full_output(idx):
     y, conv = run(inp)
     ref = reference(inp)
     assert_close(L.dtype, y, ref, L.name)
+
+
+def test_layer2_on_tensor_cores_full_output():
+    """The 640x640 stem through the three-TF32-product tensor-core kernel,
+    every output against the fp64 oracle at the fp32 tolerance."""
+    L = synthetic.LAYERS[2]
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp, algo=A_DTC)
+    assert conv.algo == A_DTC
+    assert_close(L.dtype, y, reference(inp), L.name)
 
 
 @pytest.mark.parametrize("idx,dtype", [(4, "f16"), (5, "f16"), (4, "bf16")])
@@ -114,6 +125,16 @@ SWEEP = [
     (A_TC, _L(dtype="bf16", C=64, H=9, W=72, OC=128, relu=True)),
     (A_TC, _L(dtype="bf16", C=24, D=3, H=6, W=24, OC=40, ndim=3)),
     (A_TC, _L(dtype="f16", N=3, C=200, D=2, H=5, W=240, OC=64, ndim=3)),
+    # fp32 stems on tensor cores (three TF32 products): C 1..3, strides 1..3,
+    # ragged 32-pixel groups, OC tails within a 16-channel MMA N, N > 32
+    (A_DTC, _L(C=3, H=32, W=32, OC=8)),
+    (A_DTC, _L(C=3, H=33, W=65, OC=40, stride=2, relu=True)),
+    (A_DTC, _L(C=1, H=7, W=44, OC=36)),
+    (A_DTC, _L(N=3, C=2, H=20, W=70, OC=24, pad=0)),
+    (A_DTC, _L(C=3, H=40, W=67, OC=64, stride=2, bias=False)),
+    (A_DTC, _L(C=3, H=9, W=9, OC=100, stride=3)),
+    (A_DTC, _L(C=3, H=12, W=30, OC=128, relu=True)),
+    (A_DTC, _L(C=2, H=1, W=5, OC=3)),
 ]
 
 
