@@ -238,7 +238,7 @@ def run_ours(args):
     x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
     b = torch.from_numpy(inp.b).to(dev)
     conv = Conv(x, w, b, L.stride, L.pad, L.relu)
-    launches = {gb.ALGO_DIRECT: 1, gb.ALGO_IGEMM_FFMA: 2,
+    launches = {gb.ALGO_DIRECT: 1, gb.ALGO_DIRECT_TC: 1, gb.ALGO_IGEMM_FFMA: 2,
                 gb.ALGO_IGEMM_TC: 3}[conv.algo]
     rot = Rotation(torch, conv)
 
@@ -272,10 +272,12 @@ def run_ours(args):
         stem = L.ndim == 2 and L.C <= 4 and L.k == 3 and L.stride in (1, 2)
         kernel, kfile = {gb.ALGO_DIRECT: ("direct_stem_kernel", "direct_stem.cu") if stem
                          else ("direct_conv_kernel", "direct.cu"),
-                         gb.ALGO_IGEMM_FFMA: ("igemm_ffma_kernel", "igemm_ffma.cu"),
+                         gb.ALGO_DIRECT_TC: ("stem_tf32_kernel", "stem_tf32.cuh"),
+                         gb.ALGO_IGEMM_FFMA: ("igemm_ffma2_kernel" if L.C % 16 == 0 else "igemm_ffma_kernel",
+                                              "igemm_ffma.cu"),
                          gb.ALGO_IGEMM_TC: ("igemm_tc_kernel", "igemm_tc.cu")}[conv.algo]
         kernel_key = f"{kernel}:{L.name}"
-        if conv.algo == gb.ALGO_DIRECT:
+        if conv.algo in (gb.ALGO_DIRECT, gb.ALGO_DIRECT_TC):
             achieved = L.compulsory_bytes() / avg_s / 1e9
             roof = {"bound": "hbm", "achieved": round(achieved, 1),
                     "peak": pk["hbm_gbs"], "unit": "GB/s",
