@@ -18,6 +18,7 @@ OK = 0
 ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ACT, ERR_ALIGN, ERR_WORKSPACE = 1, 2, 3, 4, 5, 6
 ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALGO = 7, 8, 9, 10
 ERR_LAYOUT, ERR_OVERLAP, ERR_CUDA, ERR_RESERVED = 11, 12, 13, 14
+TPAD_SYMMETRIC, TPAD_CAUSAL, TPAD_NONE = 0, 1, 2
 ERR_TOO_LARGE = 15
 NOALLOC_SCRATCH_BYTES = 8 << 20
 F32, F16, BF16 = 0, 1, 2
@@ -40,7 +41,7 @@ class Desc(ctypes.Structure):
                 ("k", ctypes.c_int), ("pad", ctypes.c_int),
                 ("stride", ctypes.c_int), ("dtype", ctypes.c_int),
                 ("act", ctypes.c_int), ("w_layout", ctypes.c_int),
-                ("algo", ctypes.c_int), ("reserved", ctypes.c_int),
+                ("algo", ctypes.c_int), ("flags", ctypes.c_int),
                 ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t)]
 
@@ -103,14 +104,14 @@ def _stream(s):
 
 def make_desc(N, C, H, W, OC, k, pad=0, stride=1, D=1, dtype=F32,
               act=ACT_NONE, w_layout=W_OIHW, algo=ALGO_AUTO, workspace=None,
-              workspace_bytes=0, reserved=0):
+              workspace_bytes=0, flags=0, tpad=0):
     if isinstance(dtype, str):
         dtype = DTYPES[dtype]
     d = Desc()
     d.N, d.C, d.D, d.H, d.W = N, C, D, H, W
     d.OC, d.k, d.pad, d.stride = OC, k, pad, stride
     d.dtype, d.act, d.w_layout, d.algo = dtype, act, w_layout, algo
-    d.reserved = reserved
+    d.flags = flags | tpad
     d.workspace = _ptr(workspace)
     d.workspace_bytes = workspace_bytes
     return d

@@ -24,7 +24,10 @@ bool in_range(int v, int lo, int hi) { return v >= lo && v <= hi; }
 gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (!d) return GBCONV_ERR_NULL;
     if (ndim != 2 && ndim != 3) return GBCONV_ERR_SHAPE;
-    if (d->reserved != 0) return GBCONV_ERR_RESERVED;
+    if ((d->flags & ~GBCONV_FLAG_TPAD_MASK) != 0) return GBCONV_ERR_RESERVED;
+    const int tpad = d->flags & GBCONV_FLAG_TPAD_MASK;
+    if (tpad > GBCONV_TPAD_NONE) return GBCONV_ERR_RESERVED;
+    if (ndim == 2 && tpad != GBCONV_TPAD_SYMMETRIC) return GBCONV_ERR_SHAPE;
     if (!in_range(d->dtype, GBCONV_F32, GBCONV_BF16)) return GBCONV_ERR_DTYPE;
     if (!in_range(d->act, GBCONV_ACT_NONE, GBCONV_ACT_RELU)) return GBCONV_ERR_ACT;
     if (!in_range(d->w_layout, GBCONV_W_OIHW, GBCONV_W_PACKED)) return GBCONV_ERR_LAYOUT;
@@ -42,8 +45,16 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     q.N = d->N; q.C = d->C; q.D = d->D; q.H = d->H; q.W = d->W;
     q.OC = d->OC; q.k = d->k; q.pad = d->pad; q.stride = d->stride;
     q.kd = ndim == 3 ? d->k : 1;
-    q.pad_d = ndim == 3 ? d->pad : 0;
-    int64_t od = ndim == 3 ? out_extent(d->D, d->k, d->pad, d->stride) : 1;
+    q.pad_d = q.pad_d_back = 0;
+    if (ndim == 3) {
+        q.pad_d = tpad == GBCONV_TPAD_SYMMETRIC ? d->pad : (tpad == GBCONV_TPAD_CAUSAL ? d->k - 1 : 0);
+        q.pad_d_back = tpad == GBCONV_TPAD_SYMMETRIC ? d->pad : 0;
+    }
+    int64_t od = 1;
+    if (ndim == 3) {
+        const int64_t span = (int64_t)d->D + q.pad_d + q.pad_d_back - d->k;
+        od = span < 0 ? 0 : span / d->stride + 1;
+    }
     int64_t oh = out_extent(d->H, d->k, d->pad, d->stride);
     int64_t ow = out_extent(d->W, d->k, d->pad, d->stride);
     if (od <= 0 || oh <= 0 || ow <= 0) return GBCONV_ERR_SHAPE;
@@ -326,7 +337,7 @@ const char *gbconv_status_string(gbconv_status s) {
     case GBCONV_ERR_LAYOUT: return "invalid weight layout";
     case GBCONV_ERR_OVERLAP: return "output overlaps an input or the workspace";
     case GBCONV_ERR_CUDA: return "CUDA call failed";
-    case GBCONV_ERR_RESERVED: return "reserved field not zero";
+    case GBCONV_ERR_RESERVED: return "reserved flag bit set or unknown frame-padding mode";
     case GBCONV_ERR_TOO_LARGE: return "problem needs more scratch than the fixed no-allocation array holds";
     }
     return "unknown status";

@@ -15,7 +15,8 @@ struct Problem {
     int N, C, D, H, W;        // D == 1 for 2D
     int OC, k, pad, stride;
     int kd;                   // kernel extent along D: k for 3D, 1 for 2D
-    int pad_d;                // pad along D: pad for 3D, 0 for 2D
+    int pad_d;                // zero frames before D (front): pad, k-1 (causal) or 0; 0 for 2D
+    int pad_d_back;           // zero frames after D
     int OD, OH, OW;
     int dtype, act, w_layout, algo;   // algo resolved (never AUTO)
     int taps;                 // kd * k * k

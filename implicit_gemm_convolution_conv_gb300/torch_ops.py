@@ -11,8 +11,8 @@ import torch
 
 from . import (ACT_NONE, ACT_RELU, ALGO_AUTO, BF16, F16, F32, W_OIHW,
                W_PACKED, GbconvError, check, conv2d_fwd, conv3d_fwd,
-               make_desc, select_algo, weight_pack, weight_packed_size,
-               workspace_size)
+               make_desc, output_shape, select_algo, weight_pack,
+               weight_packed_size, workspace_size)
 
 TORCH_DTYPE = {F32: torch.float32, F16: torch.float16, BF16: torch.bfloat16}
 CODE_OF = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
@@ -34,7 +34,7 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-def _desc(x, OC, k, stride, pad, relu, algo, w_layout):
+def _desc(x, OC, k, stride, pad, relu, algo, w_layout, tpad=0):
     nsp = x.dim() - 2
     if nsp == 2:
         N, C, H, W = x.shape
@@ -43,7 +43,7 @@ def _desc(x, OC, k, stride, pad, relu, algo, w_layout):
         N, C, D, H, W = x.shape
     d = make_desc(N, C, H, W, OC, k=k, pad=pad, stride=stride, D=D,
                   dtype=CODE_OF[x.dtype], act=ACT_RELU if relu else ACT_NONE,
-                  w_layout=w_layout, algo=algo)
+                  w_layout=w_layout, algo=algo, tpad=tpad)
     return d, nsp
 
 
@@ -60,11 +60,11 @@ class Conv:
     """
 
     def __init__(self, x, w, b=None, stride=1, pad=0, relu=False,
-                 algo=ALGO_AUTO, prepack=False, out=None, workspace=None):
+                 algo=ALGO_AUTO, prepack=False, out=None, workspace=None, tpad=0):
         self.x, self.b = x, b
         OC, k = w.shape[0], w.shape[-1]
         layout = W_PACKED if prepack else W_OIHW
-        self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout)
+        self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout, tpad)
         st, self.algo = select_algo(self.desc, self.nsp)
         check(st)
         if prepack:
@@ -85,7 +85,12 @@ class Conv:
             self.desc.workspace = workspace.data_ptr()
             self.desc.workspace_bytes = ws
         self.workspace = workspace
-        self.y = out if out is not None else output_tensor(x, OC, k, stride, pad)
+        if out is None:
+            st, (od, oh, ow) = output_shape(self.desc, self.nsp)
+            check(st)
+            sp = [oh, ow] if self.nsp == 2 else [od, oh, ow]
+            out = torch.empty([x.shape[0], OC] + sp, dtype=x.dtype, device=x.device)
+        self.y = out
         self._fn = conv2d_fwd if self.nsp == 2 else conv3d_fwd
 
     def with_input(self, x):
@@ -110,6 +115,6 @@ def _aligned_view(raw: torch.Tensor, nbytes: int) -> torch.Tensor:
 
 
 def forward(x, w, b=None, stride=1, pad=0, relu=False, algo=ALGO_AUTO,
-            prepack=False):
+            prepack=False, tpad=0):
     """One convolution call; returns y (allocated here)."""
-    return Conv(x, w, b, stride, pad, relu, algo, prepack)()
+    return Conv(x, w, b, stride, pad, relu, algo, prepack, tpad=tpad)()

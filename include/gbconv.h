@@ -69,7 +69,7 @@ typedef enum gbconv_status {
     GBCONV_ERR_LAYOUT = 11,            /* unknown weight layout */
     GBCONV_ERR_OVERLAP = 12,           /* y overlaps x, w, b or the workspace */
     GBCONV_ERR_CUDA = 13,              /* another CUDA runtime/driver call failed */
-    GBCONV_ERR_RESERVED = 14,          /* a reserved descriptor field is not zero */
+    GBCONV_ERR_RESERVED = 14,          /* a reserved flag bit is set, or an unknown frame-padding mode */
     GBCONV_ERR_TOO_LARGE = 15          /* gbconv_conv_fwd_noalloc: scratch need exceeds its fixed array */
 } gbconv_status;
 
@@ -101,9 +101,30 @@ typedef enum gbconv_algo {
 } gbconv_algo;
 
 /*
+ * Padding of the frame axis of conv3d (bits 0-1 of gbconv_desc.flags). The
+ * video VAE of git.erdda.com/Tencent/ncnn/discussions/7001 (SeedVR2, section
+ * 3.3) runs causal Convolution3D: an output frame sees only its own and
+ * earlier input frames, the missing leading frames being zeros on the first
+ * chunk and the previous chunk's last k-1 frames afterwards.
+ *   SYMMETRIC: `pad` zero frames before and after (the same as H and W).
+ *   CAUSAL:    k-1 zero frames before, none after; output frame t reads input
+ *              frames t*stride-(k-1) .. t*stride. OD = floor((D-1)/stride)+1.
+ *   NONE:      no frame padding (for callers that prepend the k-1 cached frames
+ *              of the previous chunk themselves). OD = floor((D-k)/stride)+1.
+ * H and W are always padded by `pad` on both sides. conv2d takes SYMMETRIC only.
+ */
+typedef enum gbconv_tpad {
+    GBCONV_TPAD_SYMMETRIC = 0,
+    GBCONV_TPAD_CAUSAL = 1,
+    GBCONV_TPAD_NONE = 2
+} gbconv_tpad;
+#define GBCONV_FLAG_TPAD_MASK 0x3
+
+/*
  * Problem descriptor. Zero-initialise it, then set every field you use.
  * Kernel size, pad and stride are the same on every spatial axis (the pages'
- * single kSize/pad/stride parameters). For conv2d, D must be 1.
+ * single kSize/pad/stride parameters); conv3d's frame axis may instead be
+ * padded causally (flags). For conv2d, D must be 1.
  */
 typedef struct gbconv_desc {
     int N, C, D, H, W;        /* input: batch, channels, frames (1 for 2D), height, width */
@@ -112,7 +133,7 @@ typedef struct gbconv_desc {
     int act;                  /* gbconv_act */
     int w_layout;             /* gbconv_wlayout */
     int algo;                 /* gbconv_algo */
-    int reserved;             /* must be 0 */
+    int flags;                /* bits 0-1: gbconv_tpad (conv3d frame padding); other bits must be 0 */
     void *workspace;          /* device scratch, >= gbconv_workspace_size bytes, 256-B aligned */
     size_t workspace_bytes;
 } gbconv_desc;

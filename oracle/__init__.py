@@ -32,10 +32,10 @@ def _lib():
         i64p = ctypes.POINTER(ctypes.c_int64)
         ci = ctypes.c_int
         lib.oracle_conv2d.argtypes = [ci] * 9 + [dp, dp, dp, dp]
-        lib.oracle_conv3d.argtypes = [ci] * 10 + [dp, dp, dp, dp]
+        lib.oracle_conv3d.argtypes = [ci] * 12 + [dp, dp, dp, dp]
         lib.oracle_conv2d_at.argtypes = ([ci] * 9 + [dp, dp, dp, i64p,
                                                      ctypes.c_int64, dp])
-        lib.oracle_conv3d_at.argtypes = ([ci] * 10 + [dp, dp, dp, i64p,
+        lib.oracle_conv3d_at.argtypes = ([ci] * 12 + [dp, dp, dp, i64p,
                                                       ctypes.c_int64, dp])
         for f in (lib.oracle_conv2d, lib.oracle_conv3d, lib.oracle_conv2d_at,
                   lib.oracle_conv3d_at, lib.oracle_threads):
@@ -107,16 +107,35 @@ def conv2d(x, w, b=None, stride=1, pad=0, relu=False, dtype=None):
     return y
 
 
-def conv3d(x, w, b=None, stride=1, pad=0, relu=False, dtype=None):
+TPAD_SYMMETRIC, TPAD_CAUSAL, TPAD_NONE = 0, 1, 2
+
+
+def frame_pads(k: int, pad: int, tpad: int):
+    """(zero frames before, after) the input for a frame-padding mode:
+    symmetric (pad, pad); causal (k-1, 0), the video VAE's causal
+    Convolution3D (git.erdda.com/Tencent/ncnn/discussions/7001, section 3.3);
+    none (0, 0) for a chunk that already carries its predecessor's frames."""
+    if tpad == TPAD_SYMMETRIC:
+        return pad, pad
+    if tpad == TPAD_CAUSAL:
+        return k - 1, 0
+    if tpad == TPAD_NONE:
+        return 0, 0
+    raise ValueError(f"unknown frame-padding mode {tpad}")
+
+
+def conv3d(x, w, b=None, stride=1, pad=0, relu=False, dtype=None, tpad=0):
     """y[n,oc,od,oy,ox] in float64 for x [N,C,D,H,W], w [OC,C,k,k,k]."""
     xd, wd, bd, k = _prep(x, w, b, dtype, 3)
     N, C, D, H, W = xd.shape
     OC = wd.shape[0]
-    OD, OH, OW = (out_extent(s, k, pad, stride) for s in (D, H, W))
+    pd0, pd1 = frame_pads(k, pad, tpad)
+    OD = (D + pd0 + pd1 - k) // stride + 1
+    OH, OW = (out_extent(s, k, pad, stride) for s in (H, W))
     if OD <= 0 or OH <= 0 or OW <= 0:
         raise ValueError("empty output")
     y = np.empty((N, OC, OD, OH, OW), np.float64)
-    rc = _lib().oracle_conv3d(N, C, D, H, W, OC, k, pad, stride,
+    rc = _lib().oracle_conv3d(N, C, D, H, W, OC, k, pad, pd0, pd1, stride,
                               int(bool(relu)), _ptr(xd), _ptr(wd),
                               None if bd is None else _ptr(bd), _ptr(y))
     if rc != 0:
@@ -124,7 +143,7 @@ def conv3d(x, w, b=None, stride=1, pad=0, relu=False, dtype=None):
     return y
 
 
-def conv_at(x, w, b, flat_idx, stride=1, pad=0, relu=False, dtype=None):
+def conv_at(x, w, b, flat_idx, stride=1, pad=0, relu=False, dtype=None, tpad=0):
     """The outputs y.flat[flat_idx] of conv2d (4D x) or conv3d (5D x) only.
 
     Computes each requested output on its own, so full-size layers can be
@@ -144,7 +163,8 @@ def conv_at(x, w, b, flat_idx, stride=1, pad=0, relu=False, dtype=None):
                                      ip, idx.shape[0], _ptr(out))
     elif nsp == 3:
         N, C, D, H, W = xd.shape
-        rc = _lib().oracle_conv3d_at(N, C, D, H, W, OC, k, pad, stride,
+        pd0, pd1 = frame_pads(k, pad, tpad)
+        rc = _lib().oracle_conv3d_at(N, C, D, H, W, OC, k, pad, pd0, pd1, stride,
                                      int(bool(relu)), _ptr(xd), _ptr(wd), bp,
                                      ip, idx.shape[0], _ptr(out))
     else:
@@ -154,8 +174,10 @@ def conv_at(x, w, b, flat_idx, stride=1, pad=0, relu=False, dtype=None):
     return out
 
 
-def conv(x, w, b=None, stride=1, pad=0, relu=False, dtype=None):
-    """conv2d for 4D x, conv3d for 5D x."""
+def conv(x, w, b=None, stride=1, pad=0, relu=False, dtype=None, tpad=0):
+    """conv2d for 4D x, conv3d for 5D x (tpad: frame-padding mode)."""
     if np.asarray(x).ndim == 4:
+        if tpad != TPAD_SYMMETRIC:
+            raise ValueError("conv2d has no frame axis")
         return conv2d(x, w, b, stride, pad, relu, dtype)
-    return conv3d(x, w, b, stride, pad, relu, dtype)
+    return conv3d(x, w, b, stride, pad, relu, dtype, tpad)

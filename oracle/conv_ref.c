@@ -20,7 +20,14 @@
  *
  * Convolution3D (git.erdda.com/Tencent/ncnn/discussions/7001, "SeedVR2 NCNN
  * Vulkan", section 3.2 "six custom layers") is the same sum with one more
- * spatial axis: time/depth, with the same kernel size, pad and stride.
+ * spatial axis: time/depth, with the same kernel size and stride. The frame
+ * axis has its own padding, pd0 zero frames before the first input frame and
+ * pd1 after the last: pd0 = pd1 = pad for the symmetric case; the video VAE's
+ * causal Convolution3D (same page, section 3.3) pads only the front, with
+ * k-1 frames (an output frame then reads its own and earlier frames), and a
+ * chunk that carries the previous chunk's frames is not padded at all.
+ * The input frame of tap kd is  id = od*stride - pd0 + kd, and the number of
+ * output frames is floor((D + pd0 + pd1 - k)/stride) + 1.
  *
  * Readings where the page is silent: a batch axis N is added in front (batch
  * stride C*H*W); the output size is floor((H + 2*pad - k)/stride) + 1 per
@@ -32,6 +39,14 @@
  */
 #include <stddef.h>
 #include <stdint.h>
+
+static int64_t out_extent2(int64_t in, int k, int p0, int p1, int stride)
+{
+    int64_t span = in + (int64_t)p0 + p1 - k;
+    if (span < 0)
+        return 0;
+    return span / stride + 1;
+}
 
 static int64_t out_extent(int64_t in, int k, int pad, int stride)
 {
@@ -71,7 +86,7 @@ static double conv2d_one(int C, int H, int W, int k, int pad, int stride,
 }
 
 /* One output element of the 3D convolution, y[n][oc][od][oy][ox]. */
-static double conv3d_one(int C, int D, int H, int W, int k, int pad,
+static double conv3d_one(int C, int D, int H, int W, int k, int pad, int pd0,
                          int stride, int relu, const double *x,
                          const double *w, const double *b, int64_t n,
                          int64_t oc, int64_t od, int64_t oy, int64_t ox)
@@ -79,7 +94,7 @@ static double conv3d_one(int C, int D, int H, int W, int k, int pad,
     double acc = 0.0;
     for (int64_t ic = 0; ic < C; ic++) {
         for (int64_t kd = 0; kd < k; kd++) {
-            int64_t id = od * stride - pad + kd;
+            int64_t id = od * stride - pd0 + kd;
             if (id < 0 || id >= D)
                 continue;
             for (int64_t ky = 0; ky < k; ky++) {
@@ -132,17 +147,18 @@ int oracle_conv2d(int N, int C, int H, int W, int OC, int k, int pad,
 
 /*
  * Full 3D convolution. x: [N][C][D][H][W], w: [OC][C][k][k][k],
- * y: [N][OC][OD][OH][OW]. Returns 0, or -1 on an invalid shape.
+ * y: [N][OC][OD][OH][OW]. pd0 / pd1: zero frames before / after the input
+ * frames. Returns 0, or -1 on an invalid shape.
  */
 int oracle_conv3d(int N, int C, int D, int H, int W, int OC, int k, int pad,
-                  int stride, int relu, const double *x, const double *w,
-                  const double *b, double *y)
+                  int pd0, int pd1, int stride, int relu, const double *x,
+                  const double *w, const double *b, double *y)
 {
-    int64_t OD = out_extent(D, k, pad, stride);
+    int64_t OD = out_extent2(D, k, pd0, pd1, stride);
     int64_t OH = out_extent(H, k, pad, stride);
     int64_t OW = out_extent(W, k, pad, stride);
-    if (N <= 0 || C <= 0 || OC <= 0 || k <= 0 || pad < 0 || OD <= 0 ||
-        OH <= 0 || OW <= 0)
+    if (N <= 0 || C <= 0 || OC <= 0 || k <= 0 || pad < 0 || pd0 < 0 ||
+        pd1 < 0 || OD <= 0 || OH <= 0 || OW <= 0)
         return -1;
     int64_t rows = (int64_t)N * OC * OD * OH;
 #pragma omp parallel for schedule(static)
@@ -152,8 +168,8 @@ int oracle_conv3d(int N, int C, int D, int H, int W, int OC, int k, int pad,
         int64_t oc = (r / (OH * OD)) % OC;
         int64_t n = r / (OH * OD * OC);
         for (int64_t ox = 0; ox < OW; ox++)
-            y[r * OW + ox] = conv3d_one(C, D, H, W, k, pad, stride, relu, x,
-                                        w, b, n, oc, od, oy, ox);
+            y[r * OW + ox] = conv3d_one(C, D, H, W, k, pad, pd0, stride, relu,
+                                        x, w, b, n, oc, od, oy, ox);
     }
     return 0;
 }
@@ -192,15 +208,15 @@ int oracle_conv2d_at(int N, int C, int H, int W, int OC, int k, int pad,
 
 /* Selected outputs of the 3D convolution (flat indices into NCDHW y). */
 int oracle_conv3d_at(int N, int C, int D, int H, int W, int OC, int k, int pad,
-                     int stride, int relu, const double *x, const double *w,
-                     const double *b, const int64_t *idx, int64_t count,
-                     double *out)
+                     int pd0, int pd1, int stride, int relu, const double *x,
+                     const double *w, const double *b, const int64_t *idx,
+                     int64_t count, double *out)
 {
-    int64_t OD = out_extent(D, k, pad, stride);
+    int64_t OD = out_extent2(D, k, pd0, pd1, stride);
     int64_t OH = out_extent(H, k, pad, stride);
     int64_t OW = out_extent(W, k, pad, stride);
-    if (N <= 0 || C <= 0 || OC <= 0 || k <= 0 || pad < 0 || OD <= 0 ||
-        OH <= 0 || OW <= 0)
+    if (N <= 0 || C <= 0 || OC <= 0 || k <= 0 || pad < 0 || pd0 < 0 ||
+        pd1 < 0 || OD <= 0 || OH <= 0 || OW <= 0)
         return -1;
     int64_t total = (int64_t)N * OC * OD * OH * OW;
     for (int64_t i = 0; i < count; i++)
@@ -214,8 +230,8 @@ int oracle_conv3d_at(int N, int C, int D, int H, int W, int OC, int k, int pad,
         int64_t od = (f / (OW * OH)) % OD;
         int64_t oc = (f / (OW * OH * OD)) % OC;
         int64_t n = f / (OW * OH * OD * OC);
-        out[i] = conv3d_one(C, D, H, W, k, pad, stride, relu, x, w, b, n, oc,
-                            od, oy, ox);
+        out[i] = conv3d_one(C, D, H, W, k, pad, pd0, stride, relu, x, w, b, n,
+                            oc, od, oy, ox);
     }
     return 0;
 }

@@ -42,6 +42,7 @@ class Layer:
     w_dist: str = "u11"         # u11 or he: N(0, 2/fan_in)
     b_dist: str = "u11"         # u11, u01_1: U[-0.1,0.1], u005: U[-0.05,0.05], none
     seed: int = 20260
+    tpad: int = 0               # conv3d frame padding: 0 symmetric, 1 causal (k-1 front), 2 none
 
     @property
     def kvol(self) -> int:
@@ -52,11 +53,13 @@ class Layer:
         return self.C * self.kvol
 
     def out_dims(self):
-        def ext(n):
-            return (n + 2 * self.pad - self.k) // self.stride + 1
+        def ext(n, p0, p1):
+            return (n + p0 + p1 - self.k) // self.stride + 1
+        p = self.pad
         if self.ndim == 3:
-            return (ext(self.D), ext(self.H), ext(self.W))
-        return (1, ext(self.H), ext(self.W))
+            f0, f1 = {0: (p, p), 1: (self.k - 1, 0), 2: (0, 0)}[self.tpad]
+            return (ext(self.D, f0, f1), ext(self.H, p, p), ext(self.W, p, p))
+        return (1, ext(self.H, p, p), ext(self.W, p, p))
 
     def x_shape(self):
         if self.ndim == 3:

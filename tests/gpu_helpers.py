@@ -33,7 +33,7 @@ def run(inp: synthetic.Inputs, algo=ALGO_AUTO, prepack=False):
     L = inp.layer
     x, w, b = device_inputs(inp)
     conv = Conv(x, w, b, stride=L.stride, pad=L.pad, relu=L.relu, algo=algo,
-                prepack=prepack)
+                prepack=prepack, tpad=L.tpad)
     y = conv()
     torch.cuda.synchronize()
     return oracle.widen(to_numpy(y), L.dtype), conv
@@ -43,9 +43,9 @@ def reference(inp: synthetic.Inputs, idx=None):
     L = inp.layer
     if idx is None:
         return oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu,
-                           L.dtype)
+                           L.dtype, tpad=L.tpad)
     return oracle.conv_at(inp.x, inp.w, inp.b, idx, L.stride, L.pad, L.relu,
-                          L.dtype)
+                          L.dtype, tpad=L.tpad)
 
 
 def errors(y, ref):

@@ -49,7 +49,7 @@ def test_desc_layout_matches_c(tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "gbconv.h"\n'
         "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(gbconv_desc),"
-        " offsetof(gbconv_desc, reserved), offsetof(gbconv_desc, workspace),"
+        " offsetof(gbconv_desc, flags), offsetof(gbconv_desc, workspace),"
         " offsetof(gbconv_desc, workspace_bytes));return 0;}\n")
     exe = tmp_path / "layout"
     cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"),
@@ -59,7 +59,7 @@ def test_desc_layout_matches_c(tmp_path):
     size, off_res, off_ws, off_wsb = map(int, subprocess.run(
         [str(exe)], capture_output=True, text=True, check=True).stdout.split())
     assert ctypes.sizeof(gb.Desc) == size
-    assert gb.Desc.reserved.offset == off_res
+    assert gb.Desc.flags.offset == off_res
     assert gb.Desc.workspace.offset == off_ws
     assert gb.Desc.workspace_bytes.offset == off_wsb
 
@@ -82,7 +82,8 @@ BAD = [
     (dict(dtype=3), gb.ERR_DTYPE), (dict(dtype=-1), gb.ERR_DTYPE),
     (dict(act=2), gb.ERR_ACT), (dict(act=-7), gb.ERR_ACT),
     (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, C=4), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, OC=129), gb.ERR_ALGO),
-    (dict(reserved=1), gb.ERR_RESERVED),
+    (dict(flags=4), gb.ERR_RESERVED), (dict(flags=3), gb.ERR_RESERVED),
+    (dict(tpad=gb.TPAD_CAUSAL), gb.ERR_SHAPE),      # conv2d: symmetric frames only
     (dict(algo=gb.ALGO_IGEMM_TC), gb.ERR_ALGO),     # tensor cores need 16-bit
     (dict(C=64, algo=gb.ALGO_DIRECT, k=15, pad=7, H=64, W=64, OC=32),
      gb.ERR_ALGO),                                  # halo does not fit smem
@@ -171,6 +172,17 @@ def test_auto_picks_tensor_core_stem_for_wide_fp32_stems():
     assert pick(C=4, OC=64, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
     assert pick(C=3, OC=160, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
     assert pick(C=3, OC=64, H=64, W=64, k=3, pad=1, stride=1, dtype=gb.F16) != gb.ALGO_DIRECT_TC
+
+
+def test_frame_padding_modes_shapes():
+    """Causal: OD = floor((D-1)/s)+1; none: floor((D-k)/s)+1; H, W unchanged."""
+    mk = lambda tp, s=1, D=5: gb.make_desc(1, 4, 6, 7, 2, k=3, pad=1, stride=s, D=D, tpad=tp)
+    assert gb.output_shape(mk(gb.TPAD_CAUSAL), 3) == (gb.OK, (5, 6, 7))
+    assert gb.output_shape(mk(gb.TPAD_CAUSAL, 2), 3) == (gb.OK, (3, 3, 4))
+    assert gb.output_shape(mk(gb.TPAD_NONE), 3) == (gb.OK, (3, 6, 7))
+    assert gb.output_shape(mk(gb.TPAD_NONE, 2, 9), 3) == (gb.OK, (4, 3, 4))
+    assert gb.output_shape(mk(gb.TPAD_NONE, 1, 2), 3)[0] == gb.ERR_SHAPE
+    assert gb.output_shape(mk(gb.TPAD_SYMMETRIC), 3) == (gb.OK, (5, 6, 7))
 
 
 def test_conv3d_shapes():

@@ -23,6 +23,7 @@ pytestmark = pytest.mark.gpu
 
 A_DIRECT, A_FFMA, A_TC = gb.ALGO_DIRECT, gb.ALGO_IGEMM_FFMA, gb.ALGO_IGEMM_TC
 A_DTC = gb.ALGO_DIRECT_TC
+CAUSAL, NOPAD = gb.TPAD_CAUSAL, gb.TPAD_NONE
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,6 +42,19 @@ def test_layer_full_output(idx):
     y, conv = run(inp)
     ref = reference(inp)
     assert_close(L.dtype, y, ref, L.name)
+
+
+def test_layer5_causal_frames_sampled_output():
+    """The video-VAE Convolution3D shape with causal frame padding (the
+    SeedVR2 decoder's conv; git.erdda.com/Tencent/ncnn/discussions/7001
+    section 3.3): 20,000 sampled outputs against the oracle."""
+    import dataclasses
+    L = dataclasses.replace(synthetic.LAYERS[5], tpad=CAUSAL)
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp)
+    assert conv.algo == A_TC and y.shape == L.y_shape()
+    idx_s = synthetic.sample_indices(L, 20000)
+    assert_close(L.dtype, y.ravel()[idx_s], reference(inp, idx_s), L.name + " causal")
 
 
 def test_layer2_on_tensor_cores_full_output():
@@ -66,11 +80,12 @@ def test_layer_sampled_output(idx, dtype):
 
 # --------------------------------------------------------- shape sweep
 def _L(dtype="f32", N=1, C=3, D=1, H=9, W=11, OC=4, k=3, pad=1, stride=1,
-       relu=False, bias=True, ndim=2, seed=1):
+       relu=False, bias=True, ndim=2, seed=1, tpad=0):
     return synthetic.Layer("sweep", N=N, C=C, D=D, H=H, W=W, OC=OC, k=k,
                            pad=pad, stride=stride, dtype=dtype, relu=relu,
                            ndim=ndim, x_dist="n01", w_dist="he",
-                           b_dist="u11" if bias else "none", seed=seed)
+                           b_dist="u11" if bias else "none", seed=seed,
+                           tpad=tpad)
 
 
 SWEEP = [
@@ -135,6 +150,15 @@ SWEEP = [
     (A_DTC, _L(C=3, H=9, W=9, OC=100, stride=3)),
     (A_DTC, _L(C=3, H=12, W=30, OC=128, relu=True)),
     (A_DTC, _L(C=2, H=1, W=5, OC=3)),
+    # conv3d frame padding: causal (k-1 zero frames in front) and none, on
+    # every kernel family that takes 3D, strides 1 and 2, k 3 and 5
+    (A_DIRECT, _L(C=2, D=5, H=7, W=9, OC=6, ndim=3, tpad=CAUSAL)),
+    (A_DIRECT, _L(C=1, D=6, H=9, W=8, OC=20, ndim=3, stride=2, tpad=NOPAD)),
+    (A_FFMA, _L(C=6, D=5, H=6, W=7, OC=12, ndim=3, tpad=CAUSAL, relu=True)),
+    (A_FFMA, _L(C=3, D=7, H=7, W=5, OC=65, ndim=3, k=5, pad=2, tpad=NOPAD)),
+    (A_TC, _L(dtype="f16", C=16, D=5, H=8, W=40, OC=32, ndim=3, tpad=CAUSAL)),
+    (A_TC, _L(dtype="bf16", C=24, D=9, H=6, W=24, OC=40, ndim=3, stride=2, tpad=CAUSAL)),
+    (A_TC, _L(dtype="f16", C=32, D=4, H=10, W=12, OC=16, ndim=3, tpad=NOPAD)),
 ]
 
 

@@ -113,3 +113,76 @@ def test_mutant_is_caught(name, tmp_path):
     so = _build_mutant(name, tmp_path)
     assert not _pins_pass(lambda x, w, b, s, p, r: _run2d(so, x, w, b, s, p,
                                                           r)), name
+
+
+# ------------------------------------------------------- conv3d frame padding
+MUTANTS_3D = {
+    "frame_front_pad_is_spatial_pad": ("int64_t id = od * stride - pd0 + kd;",
+                                       "int64_t id = od * stride - pad + kd;"),
+    "frame_front_pad_sign": ("int64_t id = od * stride - pd0 + kd;",
+                             "int64_t id = od * stride + pd0 + kd;"),
+    "frame_extent_ignores_back_pad": ("int64_t span = in + (int64_t)p0 + p1 - k;",
+                                      "int64_t span = in + (int64_t)p0 + p0 - k;"),
+}
+
+
+def _run3d(so, x, w, pad, pd0, pd1):
+    x = np.ascontiguousarray(x, np.float64)
+    w = np.ascontiguousarray(w, np.float64)
+    N, C, D, H, W = x.shape
+    OC, k = w.shape[0], w.shape[2]
+    OD = (D + pd0 + pd1 - k) + 1
+    OH, OW = H + 2 * pad - k + 1, W + 2 * pad - k + 1
+    # room for any frame count a mutant may compute; read back the true shape
+    room = N * OC * (D + 2 * max(pd0, pd1, 1) + 1) * OH * OW
+    buf = np.full(room, np.nan)
+    dp = ctypes.POINTER(ctypes.c_double)
+    rc = so.oracle_conv3d(N, C, D, H, W, OC, k, pad, pd0, pd1, 1, 0,
+                          x.ctypes.data_as(dp), w.ctypes.data_as(dp), None,
+                          buf.ctypes.data_as(dp))
+    return buf[:N * OC * OD * OH * OW].reshape(N, OC, OD, OH, OW) if rc == 0 else None
+
+
+def _pins3d_pass(run):
+    """Frame-padding pins applied to a mutant: PyTorch float64 for the causal
+    and no-padding modes."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    r = np.random.Generator(np.random.PCG64(77))
+    x = r.standard_normal((1, 2, 5, 4, 4))
+    w = r.standard_normal((2, 2, 3, 3, 3))
+    tx, tw = torch.from_numpy(x), torch.from_numpy(w)
+    for pd0, pd1, ref in [(2, 0, F.conv3d(F.pad(tx, (0, 0, 0, 0, 2, 0)), tw, padding=(0, 1, 1))),
+                          (0, 0, F.conv3d(tx, tw, padding=(0, 1, 1)))]:
+        y = run(x, w, 1, pd0, pd1)
+        if y is None or y.shape != tuple(ref.shape) or not np.allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12):
+            return False
+    return True
+
+
+def _build_mutant3d(name, tmp_path):
+    src = open(SRC).read()
+    old, new = MUTANTS_3D[name]
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-std=c99", "-O1", "-fPIC", "-shared", str(path),
+                    "-o", str(lib)], check=True, capture_output=True)
+    so = ctypes.CDLL(str(lib))
+    dp = ctypes.POINTER(ctypes.c_double)
+    so.oracle_conv3d.argtypes = [ctypes.c_int] * 12 + [dp] * 4
+    so.oracle_conv3d.restype = ctypes.c_int
+    return so
+
+
+def test_unmutated_oracle_passes_the_frame_subset():
+    assert _pins3d_pass(lambda x, w, p, a, b: oracle.conv3d(
+        x, w, None, 1, p, tpad=oracle.TPAD_CAUSAL if a else oracle.TPAD_NONE))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS_3D))
+def test_frame_mutant_is_caught(name, tmp_path):
+    so = _build_mutant3d(name, tmp_path)
+    # the mutant's own output length, so a wrong extent shows as a mismatch
+    assert not _pins3d_pass(lambda x, w, p, a, b: _run3d(so, x, w, p, a, b)), name

@@ -366,3 +366,80 @@ def test_layer_table_matches_stated_work():
                                            32 * 320 * 320) + 4 * 32
     assert L[5].compulsory_bytes() == 2 * (2 * 128 * 5 * 128 * 240 +
                                            128 * 128 * 27) + 4 * 128
+
+
+# ------------------------------------------------ conv3d frame padding modes
+def _ext_count(o, n, k=3, pad=1):
+    return sum(1 for t in range(k) if 0 <= o - pad + t < n)
+
+
+def test_causal_frames_all_ones_closed_form():
+    """All-ones input and weights, causal frame padding (k-1 zero frames
+    before, none after): output frame t sums min(t+1, k) input frames, so
+    y[t, oy, ox] = min(t+1, 3) * (in-bounds rows) * (in-bounds columns)."""
+    D, H, W = 5, 4, 5
+    y = oracle.conv3d(np.ones((1, 1, D, H, W)), np.ones((1, 1, 3, 3, 3)), None,
+                      stride=1, pad=1, tpad=oracle.TPAD_CAUSAL)
+    assert y.shape == (1, 1, D, H, W)
+    for t in range(D):
+        for oy in range(H):
+            for ox in range(W):
+                exp = min(t + 1, 3) * _ext_count(oy, H) * _ext_count(ox, W)
+                assert y[0, 0, t, oy, ox] == exp, (t, oy, ox)
+
+
+def test_causal_output_never_reads_later_frames():
+    """Changing input frames after t leaves output frames 0..t bit-identical;
+    changing frame t changes output frame t."""
+    r = _rng(31)
+    x = r.standard_normal((1, 2, 6, 5, 6))
+    w = r.standard_normal((3, 2, 3, 3, 3))
+    b = r.standard_normal(3)
+    y0 = oracle.conv3d(x, w, b, stride=1, pad=1, tpad=oracle.TPAD_CAUSAL)
+    for t in range(5):
+        x2 = x.copy()
+        x2[:, :, t + 1:] = r.standard_normal(x2[:, :, t + 1:].shape)
+        y2 = oracle.conv3d(x2, w, b, stride=1, pad=1, tpad=oracle.TPAD_CAUSAL)
+        np.testing.assert_array_equal(y2[:, :, :t + 1], y0[:, :, :t + 1])
+        x3 = x.copy()
+        x3[:, :, t] += 1.0
+        y3 = oracle.conv3d(x3, w, b, stride=1, pad=1, tpad=oracle.TPAD_CAUSAL)
+        assert not np.array_equal(y3[:, :, t], y0[:, :, t])
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+def test_frame_padding_modes_match_torch_float64(stride):
+    """Causal = PyTorch conv3d on the input with k-1 zero frames prepended and
+    no frame padding; none = PyTorch with no frame padding; symmetric = the
+    usual padding on all three axes."""
+    F = pytest.importorskip("torch.nn.functional")
+    import torch
+    r = _rng(32 + stride)
+    x = r.standard_normal((2, 3, 7, 5, 6))
+    w = r.standard_normal((4, 3, 3, 3, 3))
+    b = r.standard_normal(4)
+    tx, tw, tb = torch.from_numpy(x), torch.from_numpy(w), torch.from_numpy(b)
+    causal = F.conv3d(F.pad(tx, (0, 0, 0, 0, 2, 0)), tw, tb, stride=stride,
+                      padding=(0, 1, 1)).numpy()
+    none = F.conv3d(tx, tw, tb, stride=stride, padding=(0, 1, 1)).numpy()
+    sym = F.conv3d(tx, tw, tb, stride=stride, padding=1).numpy()
+    for mode, ref in [(oracle.TPAD_CAUSAL, causal), (oracle.TPAD_NONE, none),
+                      (oracle.TPAD_SYMMETRIC, sym)]:
+        y = oracle.conv3d(x, w, b, stride=stride, pad=1, tpad=mode)
+        assert y.shape == ref.shape, mode
+        np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+        idx = r.integers(0, y.size, 200)
+        np.testing.assert_array_equal(
+            oracle.conv_at(x, w, b, idx, stride=stride, pad=1, tpad=mode),
+            y.ravel()[idx])
+
+
+def test_frame_padding_output_lengths():
+    """OD = floor((D-1)/s)+1 causal, floor((D-k)/s)+1 none."""
+    for D, s in [(5, 1), (5, 2), (9, 2), (4, 3)]:
+        x = np.ones((1, 1, D, 4, 4))
+        w = np.ones((1, 1, 3, 3, 3))
+        assert oracle.conv3d(x, w, None, s, 1, tpad=oracle.TPAD_CAUSAL).shape[2] == (D - 1) // s + 1
+        assert oracle.conv3d(x, w, None, s, 1, tpad=oracle.TPAD_NONE).shape[2] == (D - 3) // s + 1
+    with pytest.raises(ValueError):
+        oracle.conv(np.ones((1, 1, 4, 4)), np.ones((1, 1, 3, 3)), tpad=oracle.TPAD_CAUSAL)
