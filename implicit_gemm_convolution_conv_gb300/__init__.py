@@ -31,7 +31,8 @@ SYMBOLS = ["gbconv_conv2d_fwd", "gbconv_conv3d_fwd", "gbconv_output_shape",
            "gbconv_weight_pack", "gbconv_select_algo",
            "gbconv_device_supported", "gbconv_status_string",
            "gbconv_algo_name", "gbconv_check_device_error",
-           "gbconv_set_wait_limit_ns", "gbconv_conv_fwd_noalloc"]
+           "gbconv_set_wait_limit_ns", "gbconv_conv_fwd_noalloc",
+           "gbconv_fold_batchnorm"]
 
 
 class Desc(ctypes.Structure):
@@ -75,6 +76,7 @@ def _load():
         "gbconv_check_device_error": ([P], I),
         "gbconv_set_wait_limit_ns": ([ctypes.c_uint64], I),
         "gbconv_conv_fwd_noalloc": ([DP, I, P, P, P, P, P], I),
+        "gbconv_fold_batchnorm": ([DP, I, P, P, P, P, P, P, ctypes.c_float, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -186,6 +188,16 @@ def conv_fwd_noalloc(desc, ndim, x, w, b, y, stream=None):
     return LIB.gbconv_conv_fwd_noalloc(ctypes.byref(desc), ndim, _ptr(x),
                                        _ptr(w), _ptr(b), _ptr(y),
                                        _stream(stream))
+
+
+def fold_batchnorm(desc, ndim, w, b, gamma, beta, mean, var, eps, w_out, b_out,
+                   stream=None):
+    """gbconv_fold_batchnorm: BatchNorm folded into the conv's weights and
+    bias (w_out, b_out may be w, b); returns the status code."""
+    return LIB.gbconv_fold_batchnorm(ctypes.byref(desc), ndim, _ptr(w), _ptr(b),
+                                     _ptr(gamma), _ptr(beta), _ptr(mean),
+                                     _ptr(var), float(eps), _ptr(w_out),
+                                     _ptr(b_out), _stream(stream))
 
 
 def check(status):

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgbconv.so")
-SOURCES = ["api.cu", "direct.cu", "direct_stem.cu", "igemm_ffma.cu", "igemm_tc.cu",
+SOURCES = ["api.cu", "direct.cu", "direct_stem.cu", "fold.cu", "igemm_ffma.cu", "igemm_tc.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -296,6 +296,35 @@ gbconv_status gbconv_weight_pack(const gbconv_desc *desc, int ndim,
     return GBCONV_OK;
 }
 
+gbconv_status gbconv_fold_batchnorm(const gbconv_desc *desc, int ndim, const void *w,
+                                    const float *b, const float *gamma, const float *beta,
+                                    const float *mean, const float *var, float eps,
+                                    void *w_out, float *b_out, cudaStream_t stream) {
+    Problem p;
+    gbconv_status st = build_problem(desc, ndim, &p);
+    if (st != GBCONV_OK) return st;
+    if (!w || !gamma || !beta || !mean || !var || !w_out || !b_out) return GBCONV_ERR_NULL;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return GBCONV_ERR_SHAPE;
+    if (!aligned(w, p.elt) || !aligned(w_out, p.elt) || !aligned(b_out, 4) || !aligned(gamma, 4) ||
+        !aligned(beta, 4) || !aligned(mean, 4) || !aligned(var, 4) || (b && !aligned(b, 4)))
+        return GBCONV_ERR_ALIGN;
+    const size_t wb = (size_t)p.w_elems * p.elt, vb = (size_t)p.OC * 4;
+    // w_out may be w and b_out may be b (in place); nothing else may overlap.
+    if ((w_out != w && overlap(w_out, wb, w, wb)) || (b_out != b && overlap(b_out, vb, b, b ? vb : 0)) ||
+        overlap(w_out, wb, b_out, vb) || overlap(w_out, wb, gamma, vb) || overlap(w_out, wb, beta, vb) ||
+        overlap(w_out, wb, mean, vb) || overlap(w_out, wb, var, vb) || overlap(b_out, vb, gamma, vb) ||
+        overlap(b_out, vb, beta, vb) || overlap(b_out, vb, mean, vb) || overlap(b_out, vb, var, vb) ||
+        overlap(b_out, vb, w, wb))
+        return GBCONV_ERR_OVERLAP;
+    st = device_check();
+    if (st != GBCONV_OK) return st;
+    if (launch_fold_bn(p, w, b, gamma, beta, mean, var, eps, w_out, b_out, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GBCONV_ERR_LAUNCH;
+    }
+    return GBCONV_OK;
+}
+
 gbconv_status gbconv_select_algo(const gbconv_desc *desc, int ndim, int *algo) {
     Problem p;
     gbconv_status st = build_problem(desc, ndim, &p);

@@ -72,6 +72,11 @@ cudaError_t launch_igemm_tc(const Problem &p, const void *x_cl,
                             const void *w_packed, const float *b, void *y,
                             cudaStream_t s);
 
+// BatchNorm folded into OIHW weights and an fp32 bias (fold.cu).
+cudaError_t launch_fold_bn(const Problem &p, const void *w, const float *b, const float *gamma,
+                           const float *beta, const float *mean, const float *var, float eps,
+                           void *w_out, float *b_out, cudaStream_t s);
+
 // Device-side error word and wait limit (defined in igemm_tc.cu).
 uint64_t wait_limit_ns();
 void set_wait_limit_ns(uint64_t ns);

@@ -188,6 +188,28 @@ gbconv_status gbconv_weight_pack(const gbconv_desc *desc, int ndim,
                                  const void *w_oihw, void *w_packed,
                                  cudaStream_t stream);
 
+/*
+ * Fold an inference-mode BatchNorm that follows the convolution into its
+ * weights and bias (lpnh.cn/news/2745477 section 3.1: BN folded into the
+ * conv at export, so the graph runs one conv). For each output channel oc,
+ * s = gamma[oc] / sqrt(var[oc] + eps) (fp32), and
+ *     w_out[oc][...] = w[oc][...] * s      (rounded to the storage dtype)
+ *     b_out[oc]      = (b[oc] - mean[oc]) * s + beta[oc]   (b may be NULL: 0)
+ * so a forward call with (w_out, b_out) computes
+ * gamma * (conv(x, w, b) - mean) / sqrt(var + eps) + beta (ReLU, if set in the
+ * desc, still applies after). w / w_out: OIHW/OIDHW in the desc's dtype,
+ * aligned to the element size; b, gamma, beta, mean, var, b_out: device
+ * float32 [OC]. w_out may equal w (in place) and b_out may equal b; no other
+ * overlap. eps must be finite and >= 0. Enqueued on `stream`.
+ * Errors: validation codes as for the forward call; GBCONV_ERR_NULL for a
+ * missing gamma/beta/mean/var/w/w_out/b_out; GBCONV_ERR_SHAPE for a bad eps;
+ * GBCONV_ERR_LAUNCH if the launch fails.
+ */
+gbconv_status gbconv_fold_batchnorm(const gbconv_desc *desc, int ndim, const void *w,
+                                    const float *b, const float *gamma, const float *beta,
+                                    const float *mean, const float *var, float eps,
+                                    void *w_out, float *b_out, cudaStream_t stream);
+
 /* The algorithm a forward call with this desc runs (resolves AUTO). Host only. */
 gbconv_status gbconv_select_algo(const gbconv_desc *desc, int ndim, int *algo);
 

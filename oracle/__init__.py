@@ -174,6 +174,26 @@ def conv_at(x, w, b, flat_idx, stride=1, pad=0, relu=False, dtype=None, tpad=0):
     return out
 
 
+def batchnorm(y, gamma, beta, mean, var, eps):
+    """Inference BatchNorm over the channel axis (axis 1) of y, in float64:
+    gamma * (y - mean) / sqrt(var + eps) + beta."""
+    sh = (1, -1) + (1,) * (np.asarray(y).ndim - 2)
+    g, bt, m, v = (np.asarray(a, np.float64).reshape(sh) for a in (gamma, beta, mean, var))
+    return g * (np.asarray(y, np.float64) - m) / np.sqrt(v + float(eps)) + bt
+
+
+def fold_batchnorm(w, b, gamma, beta, mean, var, eps):
+    """The BatchNorm after a conv folded into its weights and bias, in
+    float64 (lpnh.cn/news/2745477 section 3.1): s = gamma / sqrt(var + eps),
+    w' = w * s per output channel, b' = (b - mean) * s + beta (b = 0 if None)."""
+    w = np.asarray(w, np.float64)
+    s = np.asarray(gamma, np.float64) / np.sqrt(np.asarray(var, np.float64) + float(eps))
+    b0 = np.zeros(w.shape[0]) if b is None else np.asarray(b, np.float64)
+    wf = w * s.reshape((-1,) + (1,) * (w.ndim - 1))
+    bf = (b0 - np.asarray(mean, np.float64)) * s + np.asarray(beta, np.float64)
+    return wf, bf
+
+
 def conv(x, w, b=None, stride=1, pad=0, relu=False, dtype=None, tpad=0):
     """conv2d for 4D x, conv3d for 5D x (tpad: frame-padding mode)."""
     if np.asarray(x).ndim == 4:
