@@ -19,6 +19,7 @@ implementation: the pages ship no runnable code) on the same layer, on the
 host cores.
 """
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -39,6 +40,18 @@ METRIC = ("conv TFLOP/s and % of roofline per layer shape at 1 GB300 "
           "(vs CPU oracle)")
 WORKLOADS = {"detection_stem": 2, "tiny": 1, "text_line_batch": 3,
              "wide_dense_f16": 4, "video_vae_conv3d_f16": 5}
+# Variants of a layer shape: (layer, fields changed, name suffix). The fused
+# 2x2 max pool of the stem, and the video-VAE conv3d with causal frame padding.
+VARIANTS = {"detection_stem_maxpool": (2, {"pool": True}, "+maxpool2x2"),
+            "video_vae_conv3d_f16_causal": (5, {"tpad": 1}, "+causal_frames")}
+
+
+def workload_layer(name):
+    if name in WORKLOADS:
+        return synthetic.LAYERS[WORKLOADS[name]]
+    idx, kw, suffix = VARIANTS[name]
+    base = synthetic.LAYERS[idx]
+    return dataclasses.replace(base, name=base.name + suffix, **kw)
 DEFAULT_WORKLOAD = "detection_stem"
 FLUSH_BYTES = 256 << 20
 SM_COUNT_FALLBACK = 152
@@ -233,11 +246,11 @@ def run_ours(args):
         torch.cuda.synchronize()
         return [e0.elapsed_time(e1) for e0, e1 in evs]
 
-    L = synthetic.LAYERS[WORKLOADS[args.workload]]
+    L = workload_layer(args.workload)
     inp = synthetic.make_inputs(L)
     x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
     b = torch.from_numpy(inp.b).to(dev)
-    conv = Conv(x, w, b, L.stride, L.pad, L.relu)
+    conv = Conv(x, w, b, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool)
     launches = {gb.ALGO_DIRECT: 1, gb.ALGO_DIRECT_TC: 1, gb.ALGO_IGEMM_FFMA: 2,
                 gb.ALGO_IGEMM_TC: 3}[conv.algo]
     rot = Rotation(torch, conv)
@@ -377,7 +390,9 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
     back-to-back time with L2-resident buffers."""
     out = []
     p32 = fp32_peak_tflops(pk, sms)
-    for idx, L in sorted(synthetic.LAYERS.items()):
+    layers = sorted(synthetic.LAYERS.items()) + [
+        (VARIANTS[v][0], workload_layer(v)) for v in sorted(VARIANTS)]
+    for idx, L in layers:
         inp = synthetic.make_inputs(L)
         x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
         b = torch.from_numpy(inp.b).to(dev)
@@ -389,7 +404,7 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
         t_ideal = max(t_c, t_m)
         t_ideal_335 = max(t_c, L.compulsory_bytes() / 3.35e12)
         for prepack in (False, True):
-            conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack)
+            conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack, tpad=L.tpad, pool=L.pool)
             rot = Rotation(torch, conv)
             calls = 200 if idx <= 3 else (100 if idx == 4 else 40)
             for _ in range(3):
@@ -431,18 +446,25 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
     return out
 
 
+def oracle_layer(oracle, L, inp):
+    """The oracle's whole result for a layer (conv, then the 2x2 max pool
+    when the layer has one)."""
+    y = oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype, tpad=L.tpad)
+    return oracle.maxpool2(y) if L.pool else y
+
+
 def cpu_baseline(L, inp, budget_s=10.0):
     """The oracle as it stands on the host cores, on the whole layer when
     one call fits the budget, else on a sample of outputs."""
     import oracle
     threads = oracle.threads()
     t0 = time.perf_counter()
-    oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+    oracle_layer(oracle, L, inp)
     one = time.perf_counter() - t0
-    if one <= budget_s / 2:
+    if one <= budget_s / 2 or L.pool:
         reps, t0 = 0, time.perf_counter()
         while time.perf_counter() - t0 < budget_s and reps < 1000:
-            oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+            oracle_layer(oracle, L, inp)
             reps += 1
         dt = time.perf_counter() - t0
         flop = L.flops() * reps
@@ -453,7 +475,7 @@ def cpu_baseline(L, inp, budget_s=10.0):
         idx = np.random.Generator(np.random.PCG64(1)).integers(0, total, n)
         t0 = time.perf_counter()
         oracle.conv_at(inp.x, inp.w, inp.b, idx, L.stride, L.pad, L.relu,
-                       L.dtype)
+                       L.dtype, tpad=L.tpad)
         dt = time.perf_counter() - t0
         flop = L.flops() * n / total
         sample = f"{n} of {total} outputs"
@@ -467,15 +489,15 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    L = synthetic.LAYERS[WORKLOADS[args.workload]]
+    L = workload_layer(args.workload)
     inp = synthetic.make_inputs(L)
     import oracle
     threads = oracle.threads()
     for _ in range(args.warmup):
-        oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+        oracle_layer(oracle, L, inp)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu, L.dtype)
+        oracle_layer(oracle, L, inp)
     dt = time.perf_counter() - t0
     value = L.flops() * args.steps / dt / 1e12
     line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
@@ -500,7 +522,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(VARIANTS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--skip-layers", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

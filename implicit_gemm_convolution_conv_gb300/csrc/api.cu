@@ -24,7 +24,9 @@ bool in_range(int v, int lo, int hi) { return v >= lo && v <= hi; }
 gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (!d) return GBCONV_ERR_NULL;
     if (ndim != 2 && ndim != 3) return GBCONV_ERR_SHAPE;
-    if ((d->flags & ~GBCONV_FLAG_TPAD_MASK) != 0) return GBCONV_ERR_RESERVED;
+    if ((d->flags & ~(GBCONV_FLAG_TPAD_MASK | GBCONV_FLAG_MAXPOOL2)) != 0) return GBCONV_ERR_RESERVED;
+    const int pool = (d->flags & GBCONV_FLAG_MAXPOOL2) ? 1 : 0;
+    if (pool && ndim != 2) return GBCONV_ERR_SHAPE;
     const int tpad = d->flags & GBCONV_FLAG_TPAD_MASK;
     if (tpad > GBCONV_TPAD_NONE) return GBCONV_ERR_RESERVED;
     if (ndim == 2 && tpad != GBCONV_TPAD_SYMMETRIC) return GBCONV_ERR_SHAPE;
@@ -62,9 +64,13 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     q.taps = q.kd * q.k * q.k;
     q.in_vol = (int64_t)q.D * q.H * q.W;
     q.out_vol = od * oh * ow;
+    q.pool = pool;
+    q.YH = pool ? q.OH / 2 : q.OH;
+    q.YW = pool ? q.OW / 2 : q.OW;
+    if (q.YH <= 0 || q.YW <= 0) return GBCONV_ERR_SHAPE;
     q.x_elems = (int64_t)q.N * q.C * q.in_vol;
     q.w_elems = (int64_t)q.OC * q.C * q.taps;
-    q.y_elems = (int64_t)q.N * q.OC * q.out_vol;
+    q.y_elems = (int64_t)q.N * q.OC * q.OD * q.YH * q.YW;
     if (q.x_elems > GBCONV_MAX_ELEMS || q.w_elems > GBCONV_MAX_ELEMS ||
         q.y_elems > GBCONV_MAX_ELEMS)
         return GBCONV_ERR_SHAPE;
@@ -78,7 +84,9 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (algo == GBCONV_ALGO_AUTO) {
         // fp32 3x3 stems of 48+ output channels: the tensor-core stem (its
         // cost does not grow with OC up to 128; measured faster from 64).
-        if (stem_tc_supported(q) && q.OC >= 48)
+        if (q.pool)
+            algo = GBCONV_ALGO_DIRECT;          // the fused pool's only kernel
+        else if (stem_tc_supported(q) && q.OC >= 48)
             algo = GBCONV_ALGO_DIRECT_TC;
         else if ((int64_t)q.C * q.taps <= 64 && direct_supported(q))
             algo = GBCONV_ALGO_DIRECT;
@@ -92,6 +100,8 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (algo == GBCONV_ALGO_IGEMM_TC && (q.dtype == GBCONV_F32 || !tc_supported(q)))
         return GBCONV_ERR_ALGO;
     if (algo == GBCONV_ALGO_DIRECT_TC && !stem_tc_supported(q)) return GBCONV_ERR_ALGO;
+    // The fused pool lives in the few-channel 3x3 direct kernel only.
+    if (q.pool && !(algo == GBCONV_ALGO_DIRECT && stem_supported(q))) return GBCONV_ERR_ALGO;
     *p = q;
     return GBCONV_OK;
 }
@@ -239,7 +249,7 @@ gbconv_status gbconv_output_shape(const gbconv_desc *desc, int ndim, int *OD,
     gbconv_status st = build_problem(desc, ndim, &p);
     if (st != GBCONV_OK) return st;
     if (!OD || !OH || !OW) return GBCONV_ERR_NULL;
-    *OD = p.OD; *OH = p.OH; *OW = p.OW;
+    *OD = p.OD; *OH = p.YH; *OW = p.YW;
     return GBCONV_OK;
 }
 

@@ -21,6 +21,12 @@
 //    single elements otherwise;
 //  - smem reads are 16-byte vectors shared by the lanes of a pixel group;
 //    outputs leave as 16-byte stores of 4 consecutive pixels.
+// With POOL (a 2x2, stride-2 max pool fused after bias and ReLU, as page 1
+// section 4.4 fuses conv, ReLU and pooling into one shader) a warp tile is 2
+// output rows x 8 pixels: the two lane halves hold the two rows of the same
+// pixels and channels, one shuffle takes the row maximum and adjacent pixel
+// pairs in registers the column maximum, and only the pooled quarter of the
+// output is written.
 #include "dev_common.cuh"
 #include "internal.h"
 
@@ -48,8 +54,10 @@ struct StemArgs {
     const float *b;
     void *y;
     int N, H, W, OC, OH, OW, pad;
+    int YH, YW;                             // stored output (pooled when POOL)
+    int tile_rows;                          // OH, or YH with POOL
     int tiles_w, oc_blocks;
-    int tiles_per_img;                      // OH * tiles_w
+    int tiles_per_img;                      // tile_rows * tiles_w
     long long pix_tiles;                    // N * OH * tiles_w
     int warps_per_ocb;
     int relu;
@@ -83,18 +91,21 @@ struct TilePos {
     }
 };
 
-template <typename T, int C, int S, int PAD, int P, int Q, int MINB>
+template <typename T, int C, int S, int PAD, int P, int Q, int MINB, bool POOL>
 __global__ void __launch_bounds__(kWarps * 32, MINB)
 direct_stem_kernel(const StemArgs a) {
     // Lane tile: P consecutive pixels x Q output channels, the channels taken
     // as Q/2 packed pairs; a warp covers 32/Q channel groups x (P*Q/P) pixel
-    // groups = P*Q pixels x 32 channels.
+    // groups = P*Q pixels x 32 channels. With POOL the two pixel groups are
+    // two output rows of the same P pixels.
     constexpr int QP = Q / 2;
     static_assert(Q % 2 == 0 && 32 % Q == 0, "lane tile");
-    using G = StemGeom<S, P * Q>;
+    static_assert(!POOL || (Q == 2 && P % 4 == 0), "pooled tile: two rows of P pixels");
+    using G = StemGeom<S, POOL ? P : P * Q>;
     constexpr int kTilePx = G::kTilePx;
     constexpr int K = 3;
-    constexpr int kRows = C * K;
+    constexpr int kRowsPerC = POOL ? S + K : K;                 // halo rows per input channel
+    constexpr int kRows = C * kRowsPerC;
     constexpr int kBuf = kRows * G::kRowPad;                    // floats per raw buffer
     constexpr int kTasks = (kRows * G::kChunks + 31) / 32;      // 16-byte chunks per lane
     __shared__ __align__(16) float halo[kWarps][kRing][kBuf];     // halo ring
@@ -126,14 +137,14 @@ direct_stem_kernel(const StemArgs a) {
     for (int k = 0; k < kTasks; ++k) {
         const int e = lane + 32 * k;
         const int row = e / G::kChunks, ch = e - row * G::kChunks;
-        const int c = row / K, ky = row - c * K;
+        const int c = row / kRowsPerC, ky = row - c * kRowsPerC;
         t_dst[k] = e < kRows * G::kChunks ? row * G::kRowPad + 4 * ch : -1;
         t_ky[k] = ky;
         t_col[k] = 4 * ch;
         t_off[k] = (long long)c * HW + (long long)ky * a.W + 4 * ch;
     }
 
-    TilePos pf;                              // next tile to prefetch
+    TilePos pf;                              // next tile to prefetch (oh: tile row)
     pf.n = (int)(t0 / a.tiles_per_img);
     {
         const int r = (int)(t0 - (long long)pf.n * a.tiles_per_img);
@@ -144,7 +155,7 @@ direct_stem_kernel(const StemArgs a) {
 
     // Stage the halo of tile `p` into ring slot `slot_i` (zero outside x).
     auto prefetch = [&](const TilePos &p, int slot_i) {
-        const int iy0 = p.oh * S - a.pad;
+        const int iy0 = (POOL ? 2 * p.oh : p.oh) * S - a.pad;
         const int cx0 = p.tw * kTilePx * S - 4;          // input column of position 0
         if (sizeof(T) == 4 && a.vec_load) {
             const T *base = x + (long long)p.n * C * HW + (long long)iy0 * a.W + cx0;
@@ -163,7 +174,7 @@ direct_stem_kernel(const StemArgs a) {
             const T *xn = x + (long long)p.n * C * HW;
             for (int e = lane; e < kRows * G::kRowPad; e += 32) {
                 const int row = e / G::kRowPad, col = e - row * G::kRowPad;
-                const int c = row / K, ky = row - c * K;
+                const int c = row / kRowsPerC, ky = row - c * kRowsPerC;
                 const int iy = iy0 + ky, ix = cx0 + col;
                 const bool ok = iy >= 0 && iy < a.H && ix >= 0 && ix < a.W;
                 const T *src = ok ? xn + (long long)c * HW + (long long)iy * a.W + ix : x;
@@ -209,7 +220,7 @@ direct_stem_kernel(const StemArgs a) {
     for (int i = 0; i < kRing - 1; ++i) {
         if (i < ntiles) {
             prefetch(pf, i);
-            pf.advance(a.tiles_w, a.OH);
+            pf.advance(a.tiles_w, a.tile_rows);
         } else {
             cp_async_commit();
         }
@@ -223,7 +234,7 @@ direct_stem_kernel(const StemArgs a) {
         const int si = i % kRing;
         if (i + kRing - 1 < ntiles) {
             prefetch(pf, (i + kRing - 1) % kRing);
-            pf.advance(a.tiles_w, a.OH);
+            pf.advance(a.tiles_w, a.tile_rows);
         } else {
             cp_async_commit();
         }
@@ -234,14 +245,14 @@ direct_stem_kernel(const StemArgs a) {
         for (int ii = 0; ii < P; ++ii)
 #pragma unroll
             for (int jp = 0; jp < QP; ++jp) acc[ii][jp] = bp[jp];
-        const float *hb = &halo[wid][si][0] + pg * P * S;
+        const float *hb = &halo[wid][si][0] + (POOL ? pg * S * G::kRowPad : pg * P * S);
 #pragma unroll
         for (int c = 0; c < C; ++c) {
 #pragma unroll
             for (int ky = 0; ky < K; ++ky) {
                 // {x, x} operands of the packed FMA over channel pairs.
                 float2 xp[4 * kVec];
-                const float *row = hb + (c * K + ky) * G::kRowPad;
+                const float *row = hb + (c * kRowsPerC + ky) * G::kRowPad;
 #pragma unroll
                 for (int v = 0; v < kVec; ++v) {
                     const float4 q4 = *reinterpret_cast<const float4 *>(row + 4 * v);
@@ -264,39 +275,82 @@ direct_stem_kernel(const StemArgs a) {
         }
         __syncwarp();                          // dup buffer is rewritten next tile
 
-        const int owl = cur.tw * kTilePx + pg * P;
-        T *y0 = y + ((long long)cur.n * a.OC + oc_base) * plane + (long long)cur.oh * a.OW + owl;
-#pragma unroll
-        for (int j = 0; j < Q; ++j) {
-            if (oc_base + j >= a.OC) break;
-#pragma unroll
-            for (int i4 = 0; i4 < P; i4 += 4) {
-                const int ow0 = owl + i4;
-                float o[4];
-#pragma unroll
-                for (int ii = 0; ii < 4; ++ii) {
-                    const float2 v = acc[i4 + ii][j >> 1];
-                    const float r = (j & 1) ? v.y : v.x;
-                    o[ii] = a.relu ? fmaxf(r, 0.0f) : r;
-                }
-                T *yr = y0 + j * plane + i4;
-                if (a.vec_store && ow0 + 3 < a.OW) {
-                    if (sizeof(T) == 4) {
-                        *reinterpret_cast<float4 *>(yr) = make_float4(o[0], o[1], o[2], o[3]);
-                    } else {
-                        alignas(8) T h[4];
-#pragma unroll
-                        for (int ii = 0; ii < 4; ++ii) h[ii] = Storage<T>::from_float(o[ii]);
-                        *reinterpret_cast<uint2 *>(yr) = *reinterpret_cast<const uint2 *>(h);
+        if constexpr (!POOL) {
+            const int owl = cur.tw * kTilePx + pg * P;
+            T *y0 = y + ((long long)cur.n * a.OC + oc_base) * plane + (long long)cur.oh * a.OW + owl;
+    #pragma unroll
+            for (int j = 0; j < Q; ++j) {
+                if (oc_base + j >= a.OC) break;
+    #pragma unroll
+                for (int i4 = 0; i4 < P; i4 += 4) {
+                    const int ow0 = owl + i4;
+                    float o[4];
+    #pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const float2 v = acc[i4 + ii][j >> 1];
+                        const float r = (j & 1) ? v.y : v.x;
+                        o[ii] = a.relu ? fmaxf(r, 0.0f) : r;
                     }
-                } else {
+                    T *yr = y0 + j * plane + i4;
+                    if (a.vec_store && ow0 + 3 < a.OW) {
+                        if (sizeof(T) == 4) {
+                            *reinterpret_cast<float4 *>(yr) = make_float4(o[0], o[1], o[2], o[3]);
+                        } else {
+                            alignas(8) T h[4];
+    #pragma unroll
+                            for (int ii = 0; ii < 4; ++ii) h[ii] = Storage<T>::from_float(o[ii]);
+                            *reinterpret_cast<uint2 *>(yr) = *reinterpret_cast<const uint2 *>(h);
+                        }
+                    } else {
+    #pragma unroll
+                        for (int ii = 0; ii < 4; ++ii)
+                            if (ow0 + ii < a.OW) yr[ii] = Storage<T>::from_float(o[ii]);
+                    }
+                }
+            }
+        } else {
+            // Row maximum across the lane halves (rows 0 / 1), then the column
+            // maximum over pixel pairs; lanes of row 0 store 4 pooled pixels.
+            const int pw0 = cur.tw * (P / 2);                      // first pooled column
+            const long long yplane = (long long)a.YH * a.YW;
+            T *y0 = y + ((long long)cur.n * a.OC + oc_base) * yplane + (long long)cur.oh * a.YW + pw0;
 #pragma unroll
-                    for (int ii = 0; ii < 4; ++ii)
-                        if (ow0 + ii < a.OW) yr[ii] = Storage<T>::from_float(o[ii]);
+            for (int j = 0; j < Q; ++j) {
+                float pm[P / 2];
+#pragma unroll
+                for (int i = 0; i < P / 2; ++i) {
+                    float m[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 v2 = acc[2 * i + h][j >> 1];
+                        float v = (j & 1) ? v2.y : v2.x;
+                        v = a.relu ? fmaxf(v, 0.0f) : v;
+                        m[h] = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                    }
+                    pm[i] = fmaxf(m[0], m[1]);
+                }
+                if (pg != 0 || oc_base + j >= a.OC) continue;
+                T *yr = y0 + j * yplane;
+#pragma unroll
+                for (int i4 = 0; i4 < P / 2; i4 += 4) {
+                    if (a.vec_store && pw0 + i4 + 3 < a.YW) {
+                        if (sizeof(T) == 4) {
+                            *reinterpret_cast<float4 *>(yr + i4) = make_float4(pm[i4], pm[i4 + 1], pm[i4 + 2], pm[i4 + 3]);
+                        } else {
+                            alignas(8) T h[4];
+#pragma unroll
+                            for (int ii = 0; ii < 4; ++ii) h[ii] = Storage<T>::from_float(pm[i4 + ii]);
+                            *reinterpret_cast<uint2 *>(yr + i4) = *reinterpret_cast<const uint2 *>(h);
+                        }
+                    } else {
+#pragma unroll
+                        for (int ii = 0; ii < 4; ++ii)
+                            if (pw0 + i4 + ii < a.YW) yr[i4 + ii] = Storage<T>::from_float(pm[i4 + ii]);
+                    }
                 }
             }
         }
-        cur.advance(a.tiles_w, a.OH);
+        cur.advance(a.tiles_w, a.tile_rows);
     }
     cp_async_wait<0>();
 }
@@ -308,10 +362,10 @@ constexpr int kStemQ = 2;
 constexpr int kStemMinBlocks = 3;
 constexpr int kStemTilePx = kStemP * kStemQ;
 
-template <typename T, int C, int S, int PAD>
-cudaError_t launch_stem_cs(const Problem &p, const StemArgs &a0, cudaStream_t s) {
+template <typename T, int C, int S, int PAD, bool POOL>
+cudaError_t launch_stem_csp(const Problem &p, const StemArgs &a0, cudaStream_t s) {
     StemArgs a = a0;
-    auto kern = direct_stem_kernel<T, C, S, PAD, kStemP, kStemQ, kStemMinBlocks>;
+    auto kern = direct_stem_kernel<T, C, S, PAD, kStemP, kStemQ, kStemMinBlocks, POOL>;
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -329,6 +383,11 @@ cudaError_t launch_stem_cs(const Problem &p, const StemArgs &a0, cudaStream_t s)
     const int grid = (int)((total_warps + kWarps - 1) / kWarps);
     kern<<<grid, kWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+template <typename T, int C, int S, int PAD>
+cudaError_t launch_stem_cs(const Problem &p, const StemArgs &a, cudaStream_t s) {
+    return p.pool ? launch_stem_csp<T, C, S, PAD, true>(p, a, s) : launch_stem_csp<T, C, S, PAD, false>(p, a, s);
 }
 
 template <typename T, int C>
@@ -360,14 +419,17 @@ cudaError_t launch_direct_stem(const Problem &p, const void *x, const void *w, c
     StemArgs a{};
     a.x = x; a.w = w; a.b = b; a.y = y;
     a.N = p.N; a.H = p.H; a.W = p.W; a.OC = p.OC; a.OH = p.OH; a.OW = p.OW; a.pad = p.pad;
-    a.tiles_w = (p.OW + kStemTilePx - 1) / kStemTilePx;
+    a.YH = p.YH; a.YW = p.YW;
+    // Tiles: 16 pixels of one row, or (pooled) 2 rows x 8 pixels = 4 pooled pixels.
+    a.tile_rows = p.pool ? p.YH : p.OH;
+    a.tiles_w = p.pool ? (p.YW + kStemP / 2 - 1) / (kStemP / 2) : (p.OW + kStemTilePx - 1) / kStemTilePx;
     a.oc_blocks = (p.OC + kTileOc - 1) / kTileOc;
-    a.tiles_per_img = p.OH * a.tiles_w;
+    a.tiles_per_img = a.tile_rows * a.tiles_w;
     a.pix_tiles = (long long)p.N * a.tiles_per_img;
     a.relu = p.act == GBCONV_ACT_RELU;
     const int e = p.elt;
     a.vec_load = (p.W % 4 == 0) && ((uintptr_t)x % 16 == 0);
-    a.vec_store = (p.OW % 4 == 0) && ((uintptr_t)y % (4 * e) == 0);
+    a.vec_store = (p.YW % 4 == 0) && ((uintptr_t)y % (4 * e) == 0);
     switch (p.dtype) {
     case GBCONV_F32: return launch_stem_t<float>(p, a, s);
     case GBCONV_F16: return launch_stem_t<__half>(p, a, s);

@@ -21,7 +21,9 @@ struct Problem {
     int dtype, act, w_layout, algo;   // algo resolved (never AUTO)
     int taps;                 // kd * k * k
     int64_t x_elems, w_elems, y_elems;
-    int64_t out_vol;          // OD * OH * OW
+    int64_t out_vol;          // OD * OH * OW (convolution output)
+    int pool;                 // 1: 2x2 stride-2 max pool fused after the activation
+    int YH, YW;               // stored output rows / columns (OH/2, OW/2 when pooled)
     int64_t in_vol;           // D * H * W
     int elt;                  // bytes per stored element
 };

@@ -34,7 +34,7 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-def _desc(x, OC, k, stride, pad, relu, algo, w_layout, tpad=0):
+def _desc(x, OC, k, stride, pad, relu, algo, w_layout, tpad=0, pool=False):
     nsp = x.dim() - 2
     if nsp == 2:
         N, C, H, W = x.shape
@@ -43,7 +43,7 @@ def _desc(x, OC, k, stride, pad, relu, algo, w_layout, tpad=0):
         N, C, D, H, W = x.shape
     d = make_desc(N, C, H, W, OC, k=k, pad=pad, stride=stride, D=D,
                   dtype=CODE_OF[x.dtype], act=ACT_RELU if relu else ACT_NONE,
-                  w_layout=w_layout, algo=algo, tpad=tpad)
+                  w_layout=w_layout, algo=algo, tpad=tpad, pool=pool)
     return d, nsp
 
 
@@ -60,11 +60,12 @@ class Conv:
     """
 
     def __init__(self, x, w, b=None, stride=1, pad=0, relu=False,
-                 algo=ALGO_AUTO, prepack=False, out=None, workspace=None, tpad=0):
+                 algo=ALGO_AUTO, prepack=False, out=None, workspace=None, tpad=0,
+                 pool=False):
         self.x, self.b = x, b
         OC, k = w.shape[0], w.shape[-1]
         layout = W_PACKED if prepack else W_OIHW
-        self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout, tpad)
+        self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout, tpad, pool)
         st, self.algo = select_algo(self.desc, self.nsp)
         check(st)
         if prepack:
@@ -115,6 +116,6 @@ def _aligned_view(raw: torch.Tensor, nbytes: int) -> torch.Tensor:
 
 
 def forward(x, w, b=None, stride=1, pad=0, relu=False, algo=ALGO_AUTO,
-            prepack=False, tpad=0):
+            prepack=False, tpad=0, pool=False):
     """One convolution call; returns y (allocated here)."""
-    return Conv(x, w, b, stride, pad, relu, algo, prepack, tpad=tpad)()
+    return Conv(x, w, b, stride, pad, relu, algo, prepack, tpad=tpad, pool=pool)()

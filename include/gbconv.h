@@ -119,6 +119,15 @@ typedef enum gbconv_tpad {
     GBCONV_TPAD_NONE = 2
 } gbconv_tpad;
 #define GBCONV_FLAG_TPAD_MASK 0x3
+/*
+ * Bit 2 of gbconv_desc.flags: a 2x2, stride-2 max pool fused into the
+ * epilogue after bias and activation (floor mode: y is [N][OC][OH/2][OW/2];
+ * a last odd row / column is dropped), as lpnh.cn/news/2745477 section 4.4
+ * fuses conv, ReLU and pooling into one shader for small-channel layers.
+ * conv2d only, on the direct few-channel 3x3 kernel (C <= 4, stride 1 or 2,
+ * pad <= 1); other shapes or algorithms return GBCONV_ERR_ALGO.
+ */
+#define GBCONV_FLAG_MAXPOOL2 0x4
 
 /*
  * Problem descriptor. Zero-initialise it, then set every field you use.

@@ -174,6 +174,22 @@ def conv_at(x, w, b, flat_idx, stride=1, pad=0, relu=False, dtype=None, tpad=0):
     return out
 
 
+def maxpool2(y):
+    """2x2, stride-2 max pool over the last two axes, floor mode (a last odd
+    row or column is dropped): out[..., i, j] = max of y[..., 2i+a, 2j+b] over
+    a, b in {0, 1}. The pooling that lpnh.cn/news/2745477 section 4.4 fuses
+    with conv and ReLU into one shader."""
+    y = np.asarray(y, np.float64)
+    H, W = y.shape[-2] // 2, y.shape[-1] // 2
+    out = np.empty(y.shape[:-2] + (H, W), np.float64)
+    for i in range(H):
+        for j in range(W):
+            out[..., i, j] = np.maximum(
+                np.maximum(y[..., 2 * i, 2 * j], y[..., 2 * i, 2 * j + 1]),
+                np.maximum(y[..., 2 * i + 1, 2 * j], y[..., 2 * i + 1, 2 * j + 1]))
+    return out
+
+
 def batchnorm(y, gamma, beta, mean, var, eps):
     """Inference BatchNorm over the channel axis (axis 1) of y, in float64:
     gamma * (y - mean) / sqrt(var + eps) + beta."""

@@ -43,6 +43,7 @@ class Layer:
     b_dist: str = "u11"         # u11, u01_1: U[-0.1,0.1], u005: U[-0.05,0.05], none
     seed: int = 20260
     tpad: int = 0               # conv3d frame padding: 0 symmetric, 1 causal (k-1 front), 2 none
+    pool: bool = False          # 2x2 stride-2 max pool fused after the activation (2D)
 
     @property
     def kvol(self) -> int:
@@ -71,6 +72,8 @@ class Layer:
 
     def y_shape(self):
         od, oh, ow = self.out_dims()
+        if self.pool:
+            oh, ow = oh // 2, ow // 2
         if self.ndim == 3:
             return (self.N, self.OC, od, oh, ow)
         return (self.N, self.OC, oh, ow)

@@ -33,7 +33,7 @@ def run(inp: synthetic.Inputs, algo=ALGO_AUTO, prepack=False):
     L = inp.layer
     x, w, b = device_inputs(inp)
     conv = Conv(x, w, b, stride=L.stride, pad=L.pad, relu=L.relu, algo=algo,
-                prepack=prepack, tpad=L.tpad)
+                prepack=prepack, tpad=L.tpad, pool=L.pool)
     y = conv()
     torch.cuda.synchronize()
     return oracle.widen(to_numpy(y), L.dtype), conv
@@ -41,6 +41,10 @@ def run(inp: synthetic.Inputs, algo=ALGO_AUTO, prepack=False):
 
 def reference(inp: synthetic.Inputs, idx=None):
     L = inp.layer
+    if L.pool:
+        full = oracle.maxpool2(oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad,
+                                           L.relu, L.dtype))
+        return full if idx is None else full.ravel()[idx]
     if idx is None:
         return oracle.conv(inp.x, inp.w, inp.b, L.stride, L.pad, L.relu,
                            L.dtype, tpad=L.tpad)

@@ -82,7 +82,7 @@ BAD = [
     (dict(dtype=3), gb.ERR_DTYPE), (dict(dtype=-1), gb.ERR_DTYPE),
     (dict(act=2), gb.ERR_ACT), (dict(act=-7), gb.ERR_ACT),
     (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, C=4), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, OC=129), gb.ERR_ALGO),
-    (dict(flags=4), gb.ERR_RESERVED), (dict(flags=3), gb.ERR_RESERVED),
+    (dict(flags=8), gb.ERR_RESERVED), (dict(flags=3), gb.ERR_RESERVED),
     (dict(tpad=gb.TPAD_CAUSAL), gb.ERR_SHAPE),      # conv2d: symmetric frames only
     (dict(algo=gb.ALGO_IGEMM_TC), gb.ERR_ALGO),     # tensor cores need 16-bit
     (dict(C=64, algo=gb.ALGO_DIRECT, k=15, pad=7, H=64, W=64, OC=32),
@@ -172,6 +172,23 @@ def test_auto_picks_tensor_core_stem_for_wide_fp32_stems():
     assert pick(C=4, OC=64, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
     assert pick(C=3, OC=160, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
     assert pick(C=3, OC=64, H=64, W=64, k=3, pad=1, stride=1, dtype=gb.F16) != gb.ALGO_DIRECT_TC
+
+
+def test_fused_maxpool_shapes_and_limits():
+    """Pooled y is [OH/2][OW/2] (floor); the fused pool exists on the
+    few-channel 3x3 direct kernel only."""
+    mk = lambda **kw: _desc(**dict(dict(pool=True), **kw))
+    assert gb.output_shape(mk(H=32, W=32), 2) == (gb.OK, (1, 16, 16))
+    assert gb.output_shape(mk(H=9, W=11), 2) == (gb.OK, (1, 4, 5))
+    assert gb.output_shape(mk(H=640, W=640, stride=2), 2) == (gb.OK, (1, 160, 160))
+    assert gb.select_algo(mk(H=64, W=64, OC=64), 2) == (gb.OK, gb.ALGO_DIRECT)
+    assert gb.select_algo(mk(algo=gb.ALGO_IGEMM_FFMA), 2)[0] == gb.ERR_ALGO
+    assert gb.select_algo(mk(algo=gb.ALGO_DIRECT_TC, OC=64), 2)[0] == gb.ERR_ALGO
+    assert gb.select_algo(mk(C=8), 2)[0] == gb.ERR_ALGO
+    assert gb.select_algo(mk(k=5, pad=2), 2)[0] == gb.ERR_ALGO
+    assert gb.output_shape(mk(H=1, W=8, pad=0, k=1), 2)[0] == gb.ERR_SHAPE
+    d3 = gb.make_desc(1, 3, 8, 8, 4, 3, 1, 1, D=4, pool=True)
+    assert gb.output_shape(d3, 3)[0] == gb.ERR_SHAPE
 
 
 def test_frame_padding_modes_shapes():

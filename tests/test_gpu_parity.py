@@ -57,6 +57,17 @@ def test_layer5_causal_frames_sampled_output():
     assert_close(L.dtype, y.ravel()[idx_s], reference(inp, idx_s), L.name + " causal")
 
 
+def test_layer2_with_fused_maxpool_full_output():
+    """The 640x640 stem with its 2x2 max pool fused into the epilogue:
+    every pooled output against max-pool(conv) of the oracle."""
+    import dataclasses
+    L = dataclasses.replace(synthetic.LAYERS[2], pool=True)
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp)
+    assert conv.algo == A_DIRECT and y.shape == L.y_shape() == (1, 32, 160, 160)
+    assert_close(L.dtype, y, reference(inp), L.name + " + maxpool")
+
+
 def test_layer2_on_tensor_cores_full_output():
     """The 640x640 stem through the three-TF32-product tensor-core kernel,
     every output against the fp64 oracle at the fp32 tolerance."""
@@ -80,12 +91,12 @@ def test_layer_sampled_output(idx, dtype):
 
 # --------------------------------------------------------- shape sweep
 def _L(dtype="f32", N=1, C=3, D=1, H=9, W=11, OC=4, k=3, pad=1, stride=1,
-       relu=False, bias=True, ndim=2, seed=1, tpad=0):
+       relu=False, bias=True, ndim=2, seed=1, tpad=0, pool=False):
     return synthetic.Layer("sweep", N=N, C=C, D=D, H=H, W=W, OC=OC, k=k,
                            pad=pad, stride=stride, dtype=dtype, relu=relu,
                            ndim=ndim, x_dist="n01", w_dist="he",
                            b_dist="u11" if bias else "none", seed=seed,
-                           tpad=tpad)
+                           tpad=tpad, pool=pool)
 
 
 SWEEP = [
@@ -159,6 +170,16 @@ SWEEP = [
     (A_TC, _L(dtype="f16", C=16, D=5, H=8, W=40, OC=32, ndim=3, tpad=CAUSAL)),
     (A_TC, _L(dtype="bf16", C=24, D=9, H=6, W=24, OC=40, ndim=3, stride=2, tpad=CAUSAL)),
     (A_TC, _L(dtype="f16", C=32, D=4, H=10, W=12, OC=16, ndim=3, tpad=NOPAD)),
+    # conv + bias + ReLU + 2x2 max pool in one kernel (few-channel 3x3):
+    # strides 1/2, pad 0/1, C 1..4, odd rows / columns (floor mode), OC tails,
+    # a pooled width not divisible by 4, no ReLU, f16 / bf16
+    (A_DIRECT, _L(C=3, H=32, W=32, OC=32, relu=True, pool=True)),
+    (A_DIRECT, _L(C=3, H=45, W=70, OC=40, stride=2, relu=True, pool=True)),
+    (A_DIRECT, _L(C=1, H=9, W=11, OC=5, pool=True)),
+    (A_DIRECT, _L(N=2, C=4, H=17, W=26, OC=64, pad=0, pool=True, relu=True)),
+    (A_DIRECT, _L(C=2, H=6, W=38, OC=33, stride=2, pool=True, bias=False)),
+    (A_DIRECT, _L(dtype="f16", C=3, H=40, W=64, OC=32, stride=2, relu=True, pool=True)),
+    (A_DIRECT, _L(dtype="bf16", C=3, H=21, W=30, OC=8, pool=True)),
 ]
 
 

@@ -443,3 +443,21 @@ def test_frame_padding_output_lengths():
         assert oracle.conv3d(x, w, None, s, 1, tpad=oracle.TPAD_NONE).shape[2] == (D - 3) // s + 1
     with pytest.raises(ValueError):
         oracle.conv(np.ones((1, 1, 4, 4)), np.ones((1, 1, 3, 3)), tpad=oracle.TPAD_CAUSAL)
+
+
+# ------------------------------------------------------------- max pool 2x2
+def test_maxpool2_handworked_and_floor_mode():
+    y = np.array([[1., 5., 2., 0., 9.],
+                  [3., 4., 8., 7., 9.],
+                  [6., 0., 1., 2., 9.]])[None, None]
+    np.testing.assert_array_equal(oracle.maxpool2(y)[0, 0], [[5., 8.]])
+
+
+def test_maxpool2_matches_torch():
+    F = pytest.importorskip("torch.nn.functional")
+    import torch
+    r = _rng(51)
+    for shape in [(2, 3, 8, 10), (1, 4, 7, 9), (1, 1, 2, 2)]:
+        y = r.standard_normal(shape)
+        ref = F.max_pool2d(torch.from_numpy(y), 2, 2).numpy()
+        np.testing.assert_array_equal(oracle.maxpool2(y), ref)
