@@ -82,11 +82,12 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     // 16-bit storage, exact fp32 FMA on CUDA cores for fp32.
     int algo = d->algo;
     if (algo == GBCONV_ALGO_AUTO) {
-        // fp32 3x3 stems of 48+ output channels: the tensor-core stem (its
-        // cost does not grow with OC up to 128; measured faster from 64).
+        // fp32 3x3 stems of 16+ output channels: the tensor-core stem
+        // (measured faster than the CUDA-core stem from 16 to 128 channels
+        // on 640 x 640 images, stride 1 and 2).
         if (q.pool)
             algo = GBCONV_ALGO_DIRECT;          // the fused pool's only kernel
-        else if (stem_tc_supported(q) && q.OC >= 48)
+        else if (stem_tc_supported(q) && q.OC >= 16)
             algo = GBCONV_ALGO_DIRECT_TC;
         else if ((int64_t)q.C * q.taps <= 64 && direct_supported(q))
             algo = GBCONV_ALGO_DIRECT;

@@ -25,6 +25,18 @@ template <> struct Storage<__nv_bfloat16> {
     static __device__ __forceinline__ __nv_bfloat16 from_float(float v) { return __float2bfloat16_rn(v); }
 };
 
+// Programmatic dependent launch. Kernels are launched with the programmatic
+// stream-serialization attribute, so a kernel may begin (launch, shared
+// memory and TMEM set-up) while the previous kernel in the stream is still
+// finishing. Every thread waits for the previous kernel to complete, and its
+// writes to be visible, before its first access to global memory; each
+// kernel allows its successor to launch as soon as it has started. Without
+// the attribute both instructions do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Fused epilogue (lpnh.cn/news/2745477 section 2.2: bias added at write-back;
 // section 4.4: ReLU fused into the same write): v = acc + b, then max(v, 0).
 __device__ __forceinline__ float epilogue(float acc, float bias, int relu) {

@@ -605,9 +605,7 @@ cudaError_t launch_igemm_tc(const Problem &p, const void *xc, const void *wp, co
 }
 
 bool stem_tc_supported(const Problem &p) {
-    return p.ndim == 2 && p.dtype == GBCONV_F32 && p.k == 3 && p.C <= 3 &&
-           (int64_t)p.N * p.OH * ((p.OW + 31) / 32) < (1ll << 33) &&
-           p.OC <= kStemMaxOC;
+    return p.ndim == 2 && p.dtype == GBCONV_F32 && p.k == 3 && p.C <= kStemMaxC && p.OC <= kStemMaxOC;
 }
 
 cudaError_t launch_stem_tc(const Problem &p, const void *x, const void *w, const float *b, void *y,
@@ -617,7 +615,8 @@ cudaError_t launch_stem_tc(const Problem &p, const void *x, const void *w, const
     switch (p.C) {
     case 1: return launch_stem_tf32_c<1>(p, xf, wf, b, yf, s);
     case 2: return launch_stem_tf32_c<2>(p, xf, wf, b, yf, s);
-    default: return launch_stem_tf32_c<3>(p, xf, wf, b, yf, s);
+    case 3: return launch_stem_tf32_c<3>(p, xf, wf, b, yf, s);
+    default: return launch_stem_tf32_c<4>(p, xf, wf, b, yf, s);
     }
 }
 

@@ -51,7 +51,7 @@ Workspace workspace_layout(const Problem &p);
 bool direct_supported(const Problem &p);
 bool stem_supported(const Problem &p);   // few-channel 3x3 direct kernel
 bool tc_supported(const Problem &p);
-bool stem_tc_supported(const Problem &p);   // fp32, 2D, k = 3, C <= 3: tensor cores, 3 TF32 products
+bool stem_tc_supported(const Problem &p);   // fp32, 2D, k = 3, C <= 4, OC <= 128: tensor cores, split TF32
 
 // Kernel launchers (each returns a cudaError_t from the launch).
 cudaError_t launch_direct(const Problem &p, const void *x, const void *w_oihw,
@@ -78,6 +78,24 @@ cudaError_t launch_igemm_tc(const Problem &p, const void *x_cl,
 cudaError_t launch_fold_bn(const Problem &p, const void *w, const float *b, const float *gamma,
                            const float *beta, const float *mean, const float *var, float eps,
                            void *w_out, float *b_out, cudaStream_t s);
+
+// Launch with the programmatic stream-serialization attribute (the kernel
+// calls pdl_wait() before its first global-memory access).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
 
 // Device-side error word and wait limit (defined in igemm_tc.cu).
 uint64_t wait_limit_ns();

@@ -1,64 +1,84 @@
-// fp32 convolution with a short reduction (C * 3 * 3 <= 32 taps: image
-// stems) on the tcgen05 tensor cores, each fp32 product carried by three
-// TF32 products.
+// fp32 convolution with a short reduction (C * 3 * 3 <= 36 taps: image
+// stems) on the tcgen05 tensor cores, in TF32 with split operands.
 //
 // The operation is the output-stationary sum of lpnh.cn/news/2745477 section
 // 2.2 (zero padding, bias, ReLU fused into the write-back as in section 4.4),
-// cast as a GEMM per 128-pixel tile: D[pixel][oc] = sum_k A[pixel][k] B[oc][k]
-// with k = (c, ky, kx), K = C * 9 padded to 32 (one 128-byte row per pixel).
-// Every fp32 value v is split as v = hi + lo with hi = v with its 13 low
+// cast as a GEMM per tile of 128 output pixels:
+//   y[pixel][oc] = sum_t x[pixel][t] * w[oc][t],   t = (c, ky, kx), T = C * 9.
+// Every fp32 value v is split as v = hi + lo: hi is v with its 13 low
 // mantissa bits cleared (exactly representable in TF32) and lo = v - hi
-// (exact in fp32; the MMA reads its top 19 bits). The tile accumulates
-// x_hi*w_lo + x_lo*w_hi + x_hi*w_hi in fp32 in TMEM; the dropped x_lo*w_lo
-// and the TF32 reading of lo leave a relative error near 2^-20 per product,
-// far inside the fp32 parity tolerance (rel. L2 1e-5). This split-product
-// scheme is the usual way to run fp32 GEMMs on TF32 units.
+// (exact in fp32; the MMA reads its top 19 bits). The splits are laid along
+// K and N:
+//   A[pixel][k] = [ x_hi | x_lo ]                      K = 2T (padded to 8)
+//   B[n][k]     = [ w_hi | w_hi ]  for n <  OCP
+//                 [ w_lo | w_lo ]  for n >= OCP        N = 2 * OCP
+// so that one chain of K/8 MMAs leaves x.w_hi in TMEM column oc and x.w_lo in
+// column OCP + oc; their sum is the fp32 product sum up to a relative error
+// near 2^-20 per term (the TF32 reading of lo), far inside the fp32 parity
+// tolerance (rel. L2 1e-5). Splitting fp32 products into TF32 pieces is the
+// usual way to run fp32 GEMMs on TF32 units; carrying the pieces in K and N
+// of one chain keeps the MMA count at K/8 (7 for three channels).
 //
-// On the CUDA cores this layer costs as much FP32 FMA time as HBM time, and
-// the packed FMA needs a register move per input value; on the tensor cores
-// the arithmetic is a few hundred cycles per tile and the kernel is left
-// with its memory traffic: x read once (L1 absorbs the 2.25x tap overlap at
-// stride 2) and y written once with warp-coalesced 128-byte stores.
+// GEMM orientation: M = 128 output pixels, N = 2 * OCP (OCP = OC rounded up
+// to 16). A kernel that uses TMEM is resident once per SM, so one persistent
+// CTA per SM runs G independent groups of 128 threads (G = 4 when shared
+// memory and the 512 TMEM columns allow), each with its own pixel operand,
+// accumulator and barriers; the groups overlap one another's loads, MMAs and
+// stores. The weight operand is split once per CTA and shared. Thread i of a
+// group owns pixel i of the group's tile: it splits its pixel's T taps into
+// row i of A (K-major, 128-byte swizzle), one thread of the group issues the
+// MMAs and commits to an mbarrier, and the thread then reads its own TMEM
+// lane (row i of D), adds the two halves and the bias and applies ReLU.
 //
-// GEMM orientation: M = output channels (rows of the weight operand, padded
-// with zero rows to 128), N = 256 pixels, K = 32. A tcgen05.mma costs the
-// issuing thread tens of cycles whatever its size, so the tile is shaped for
-// N = 256 (128 cycles of tensor work per instruction) rather than M = pixels
-// with N = 32 output channels (16 cycles of work, issue-bound); the zero
-// weight rows are the price.
-//
-// One persistent CTA per SM (kernels that use TMEM run one CTA per SM), 8
-// warps. A tile = 256 pixels = 8 groups of 32 consecutive output pixels of
-// one row, taken round-robin over the CTAs; thread i owns pixel i. Per tile:
-// each thread splits its pixel's taps and writes row i of the hi and lo
-// pixel operands (128-byte swizzle, two buffers); one thread issues the 12
-// MMAs (3 products x 4 K-steps of 8) into one of two TMEM accumulators
-// (256 columns each) and commits; the next tile's tap loads go out; then the
-// previous tile's epilogue: warp w reads output channels 32*(w%4) .. (its
-// TMEM lane quadrant) for 4 of the 8 pixel groups, adds the bias, applies
-// ReLU, writes each 32-channel x 32-pixel block to a staging tile (128-byte
-// swizzle) and issues a TMA tensor store (bulk, clipped at the output's
-// edges). The 8 staging tiles are shared out among the warps that hold real
-// channels, so a warp cycles through up to 4 of them without waiting for
-// its previous store. The weight operand is split once per CTA.
+// Two ways in and out of HBM:
+// - TMA (input and output rows 16-byte aligned, stride <= 3): a tile is 2
+//   output rows x 64 pixels. Its input halo (C x (s + 3) rows x 4-aligned
+//   columns, zero filled outside the image: the padding) comes in as one TMA
+//   box two tiles ahead of use, into a ring of two buffers per group; the
+//   taps are read from shared memory. The results are staged as [oc][row]
+//   [pixel] in the group's operand buffer (free once the MMAs are done) and
+//   leave as TMA tensor stores, clipped at the image edges, which drain while
+//   the group builds its next tile.
+// - Plain loads and stores otherwise: a tile is 128 consecutive pixels in
+//   (n, oh, ow) order; each thread loads its taps from global memory (the next
+//   tile's go out before the wait on the MMAs) and stores its pixel of every
+//   channel (a warp writes 128 contiguous bytes per channel).
 
-constexpr int kStemTcPx = 256;               // pixels per tile (MMA N)
-constexpr int kStemTcK = 32;                 // padded reduction (tf32 per 128-byte row)
-constexpr int kStemTcM = 128;                // MMA M: output channels padded to 128
-constexpr int kStemTcThreads = 256;
-constexpr int kStemMaxOC = 128;
+constexpr int kStemPxM = 128;                // pixels per tile (MMA M, TMEM lanes)
+constexpr int kStemPxThreads = 128;          // threads per group
+constexpr int kStemMaxOC = 128;              // MMA N = 2 * OCP <= 256
+constexpr int kStemMaxC = 4;
+constexpr int kStemMaxGroups = 4;
+constexpr size_t kStemSmemLimit = 227 * 1024;
+constexpr int kStemTileW = 64, kStemTileR = 2;   // TMA tiles: 2 output rows x 64 pixels
+constexpr int kStemMaxTmaStride = 3;             // halo box width <= 256 columns
 
 struct StemTcArgs {
     const float *x, *w, *b;
     float *y;
     int H, W, OC, OH, OW, pad, stride;
-    int groups_w;              // 32-pixel groups per output row
-    long long groups;          // N * OH * groups_w
-    long long tiles;           // ceil(groups / 8)
-    uint32_t idesc, tmem_cols;
+    int ocp;                   // OC rounded up to 16
+    long long ohw;             // OH * OW
+    long long npix;            // N * OH * OW
+    long long tiles;
+    int tiles_w, tiles_h;      // TMA tiling: 64-pixel column blocks, row pairs
+    int hd;                    // TMA: halo column of input column ow0 * s - pad (0..3)
+    int hbw, hbh;              // TMA: halo box width (multiple of 4) and height
+    uint32_t halo_box_bytes;   // TMA: C * hbh * hbw * 4
+    uint32_t halo_bytes;       // one halo buffer, 1024-aligned
+    uint32_t region_bytes;     // per group: pixel operand (and, with TMA, the output staging tile)
+    int ybox_c;                // TMA: channels per output box
+    uint32_t idesc, tmem_cols; // tmem_cols: all groups
+    int groups;                // 128-thread groups per CTA (1, 2 or 4)
     int relu;
-    int tma_store;             // output rows 16-byte aligned: TMA tensor stores
     long long wait_limit_cycles;
+};
+
+template <int C>
+struct StemShape {
+    static constexpr int T = C * 9;                   // taps
+    static constexpr int KP = (2 * T + 7) / 8 * 8;    // K: hi and lo taps, MMA steps of 8
+    static constexpr int KCH = (KP + 31) / 32;        // 128-byte chunks per operand row
 };
 
 __device__ __forceinline__ void tf32_split(float v, float &hi, float &lo) {
@@ -66,52 +86,78 @@ __device__ __forceinline__ void tf32_split(float v, float &hi, float &lo) {
     lo = v - hi;
 }
 
-// Row `r` of the hi and lo K-major 128-byte-swizzle tiles from 32 fp32
-// values (8 chunks of 4 floats, chunk j at (j ^ (r & 7)) * 16).
-__device__ __forceinline__ void store_split_row(uint32_t hi_tile, uint32_t lo_tile, int r,
-                                                const float (&v)[kStemTcK]) {
+// Row r of a K-major operand in the 128-byte swizzle layout: 16-byte unit u
+// lies in chunk u / 8 (chunks `chunk_bytes` apart) at r * 128 + ((u % 8) ^
+// (r % 8)) * 16.
+template <int KP>
+__device__ __forceinline__ void store_operand_row(uint32_t tile, uint32_t chunk_bytes, int r,
+                                                  const float (&v)[KP]) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) tf32_split(v[4 * j + e], h[e], l[e]);
-        const uint32_t off = (uint32_t)r * 128u + (uint32_t)((j ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(hi_tile + off), "f"(h[0]), "f"(h[1]),
-                     "f"(h[2]), "f"(h[3])
-                     : "memory");
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(lo_tile + off), "f"(l[0]), "f"(l[1]),
-                     "f"(l[2]), "f"(l[3])
+    for (int u = 0; u < KP / 4; ++u) {
+        const uint32_t off = (uint32_t)(u / 8) * chunk_bytes + (uint32_t)r * 128u +
+                             (uint32_t)(((u & 7) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(tile + off), "f"(v[4 * u]),
+                     "f"(v[4 * u + 1]), "f"(v[4 * u + 2]), "f"(v[4 * u + 3])
                      : "memory");
     }
 }
 
-struct StemPix {
-    int n, oh, ow0, ow;
-    bool group_ok, valid;
+// Row `row` of the pixel operand from the pixel's taps: [hi | lo | 0 pad].
+template <int C>
+__device__ __forceinline__ void store_pixel_row(uint32_t sA, int row, const float (&xv)[C * 9]) {
+    using S = StemShape<C>;
+    float v[S::KP];
+#pragma unroll
+    for (int t = 0; t < S::T; ++t) tf32_split(xv[t], v[t], v[S::T + t]);
+#pragma unroll
+    for (int t = 2 * S::T; t < S::KP; ++t) v[t] = 0.0f;
+    store_operand_row<S::KP>(sA, 16384u, row, v);
+}
+
+// The K/8 MMAs of one tile (one thread).
+template <int KP>
+__device__ __forceinline__ void stem_mmas(uint32_t tacc, uint32_t sA, uint32_t sB, uint32_t bchunk,
+                                          uint32_t idesc) {
+#pragma unroll
+    for (int s = 0; s < KP / 8; ++s) {
+        // K-step of 8 tf32 = 32 bytes = descriptor start address + 2.
+        const uint64_t ad = sw128_kmajor_desc(sA + (uint32_t)(s / 4) * 16384u) + 2u * (s % 4);
+        const uint64_t bd = sw128_kmajor_desc(sB + (uint32_t)(s / 4) * bchunk) + 2u * (s % 4);
+        tc_mma_tf32(tacc, ad, bd, idesc, s > 0);
+    }
+}
+
+// Bounded wait by lane 0 of each warp, result shared with the warp; an
+// expired wait sets the device error word.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long limit) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, limit, nullptr);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok && (threadIdx.x & 31) == 0) atomicOr(&g_device_error, 1u);
+    return ok != 0;
+}
+
+struct StemPixel {
+    long long n;
+    int rem;                   // oh * OW + ow
+    bool valid;
 };
-// Pixel `lane` of group `grp` (0..7) of tile `tile`.
-__device__ __forceinline__ StemPix stem_pixel(const StemTcArgs &a, long long tile, int grp, int lane) {
-    StemPix p{0, 0, 0, 0, false, false};
-    const long long g = tile * 8 + grp;
-    if (tile < a.tiles && g < a.groups) {
-        const int gw = (int)(g % a.groups_w);
-        const long long t = g / a.groups_w;
-        p.oh = (int)(t % a.OH);
-        p.n = (int)(t / a.OH);
-        p.ow0 = gw * 32;
-        p.ow = p.ow0 + lane;
-        p.group_ok = true;
-        p.valid = p.ow < a.OW;
+__device__ __forceinline__ StemPixel stem_pixel(const StemTcArgs &a, long long f) {
+    StemPixel p{0, 0, f < a.npix};
+    if (p.valid) {
+        p.n = f / a.ohw;
+        p.rem = (int)(f - p.n * a.ohw);
     }
     return p;
 }
 
-// The pixel's C*9 taps (zero outside the input and beyond C*9).
+// The pixel's T taps in (c, ky, kx) order from global memory, zero outside the input.
 template <int C>
-__device__ __forceinline__ void stem_gather(const StemTcArgs &a, const StemPix &p, float (&v)[kStemTcK]) {
+__device__ __forceinline__ void stem_gather(const StemTcArgs &a, const StemPixel &p, float (&v)[C * 9]) {
+    const int oh = p.rem / a.OW, ow = p.rem - oh * a.OW;
     const long long HW = (long long)a.H * a.W;
-    const float *xn = a.x + (long long)p.n * C * HW;
-    const int iy0 = p.oh * a.stride - a.pad, ix0 = p.ow * a.stride - a.pad;
+    const float *xn = a.x + p.n * C * HW;
+    const int iy0 = oh * a.stride - a.pad, ix0 = ow * a.stride - a.pad;
 #pragma unroll
     for (int c = 0; c < C; ++c)
 #pragma unroll
@@ -125,171 +171,285 @@ __device__ __forceinline__ void stem_gather(const StemTcArgs &a, const StemPix &
                 v[(c * 3 + ky) * 3 + kx] = (row_ok && (unsigned)ix < (unsigned)a.W) ? __ldg(xr + ix) : 0.0f;
             }
         }
-#pragma unroll
-    for (int q = C * 9; q < kStemTcK; ++q) v[q] = 0.0f;
 }
 
-template <int C>
-__global__ void __launch_bounds__(kStemTcThreads, 1)
-stem_tf32_kernel(const __grid_constant__ CUtensorMap tmY, const StemTcArgs a) {
-    constexpr int KT = C * 9;                           // real taps
-    static_assert(KT <= kStemTcK, "taps");
+// TMA tile t: image, first output row, first output column.
+struct StemTile {
+    int n, oh0, ow0;
+};
+__device__ __forceinline__ StemTile stem_tile(const StemTcArgs &a, long long t) {
+    StemTile s;
+    s.ow0 = (int)(t % a.tiles_w) * kStemTileW;
+    const long long r = t / a.tiles_w;
+    s.oh0 = (int)(r % a.tiles_h) * kStemTileR;
+    s.n = (int)(r / a.tiles_h);
+    return s;
+}
+// The input halo of TMA tile t as one box: columns from ow0 * s - pad - hd
+// (a multiple of 4), rows from oh0 * s - pad, all C channels of image n.
+__device__ __forceinline__ void stem_load_halo(const CUtensorMap *tmX, const StemTcArgs &a, long long t,
+                                               uint32_t dst, uint32_t bar) {
+    const StemTile s = stem_tile(a, t);
+    mbar_arrive_expect_tx(bar, a.halo_box_bytes);
+    tma_load_4d(dst, tmX, bar, s.ow0 * a.stride - a.pad - a.hd, s.oh0 * a.stride - a.pad, 0, s.n);
+}
+
+template <int C, bool TMA>
+__global__ void __launch_bounds__(kStemPxThreads * kStemMaxGroups, 1)
+stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                 const StemTcArgs a) {
+    using S = StemShape<C>;
+    constexpr int T = S::T, KP = S::KP, KCH = S::KCH;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    // Weight operand hi / lo (128 rows each), pixel operand buffers 0 / 1
-    // (hi 32 KB + lo 32 KB each), per-warp 4 KB output staging, bias, barriers.
-    const uint32_t sWh = base, sWl = base + 16384u;
-    const uint32_t sP = base + 32768u;
-    const uint32_t sY = sP + 2u * 65536u;
-    const uint32_t sBar = sY + 4096u * (kStemTcThreads / 32);
-    const uint32_t slot_addr = sBar + 16u;
-    float *sBias = reinterpret_cast<float *>(smem_raw + (slot_addr + 16u - raw));
+    const int G = a.groups;
+    const int nrows = 2 * a.ocp;                            // B rows = MMA N
+    const uint32_t bchunk = (uint32_t)nrows * 128u;
+    // Weight operand (KCH chunks of nrows x 128 B); per group its region
+    // (pixel operand, KCH chunks of 128 rows x 128 B; with TMA also the
+    // output staging tile); with TMA two halo buffers per group; per group an
+    // MMA barrier and two halo barriers; the TMEM address; the bias.
+    const uint32_t sB = base;
+    const uint32_t sR0 = sB + (uint32_t)KCH * bchunk;
+    const uint32_t sH0 = sR0 + (uint32_t)G * a.region_bytes;
+    const uint32_t sBar0 = sH0 + (TMA ? 2u * (uint32_t)G * a.halo_bytes : 0u);
+    const uint32_t slot_addr = sBar0 + 24u * (uint32_t)G;
+    float *sBias = reinterpret_cast<float *>(smem_raw + (((slot_addr + 4u + 15u) & ~15u) - raw));   // 16-byte aligned
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem_raw + (slot_addr - raw));
 
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    if (tid == 0) {
-        mbar_init(sBar, 1);
-        mbar_init(sBar + 8u, 1);
+    const int tid = threadIdx.x;
+    const int g = tid / kStemPxThreads, gtid = tid % kStemPxThreads;   // group, pixel row in the tile
+    const int q = gtid / 32;                                // TMEM lane quadrant (warp id % 4)
+    const uint32_t sA = sR0 + (uint32_t)g * a.region_bytes;
+    const uint32_t barM = sBar0 + 24u * (uint32_t)g, barH = barM + 8u;   // halo barriers barH, barH + 8
+    const uint32_t sHalo = sH0 + 2u * (uint32_t)g * a.halo_bytes;
+    // The CTA's tiles are a contiguous range (5 or 6 of the 800 tiles of a
+    // 640 x 640 stride-2 stem on 152 SMs), dealt round-robin to its groups.
+    const long long tend = (long long)(blockIdx.x + 1) * a.tiles / gridDim.x;
+    const long long tstep = G;
+    long long tile = (long long)blockIdx.x * a.tiles / gridDim.x + g;
+    const bool active = tile < tend;
+
+    pdl_launch_dependents();
+    // Per halo buffer, 1 + the barrier phase parity of a TMA load issued and
+    // not yet seen complete (0: none); kept by the group's thread 0.
+    uint32_t halo_pending[2] = {0, 0};
+    StemPixel px{};
+    float xv[T];
+    if (gtid == 0) {
+        mbar_init(barM, 1);
+        if (TMA) {
+            mbar_init(barH, 1);
+            mbar_init(barH + 8u, 1);
+        }
         fence_mbar_init();
+        if (TMA) prefetch_tmap(&tmX);
     }
-    if (warp == 0) {
+    if (tid < 32) {
         tmem_alloc(slot_addr, a.tmem_cols);
         tmem_relinquish();
     }
-    const long long tstep = gridDim.x;
-    long long tile = blockIdx.x;
-
-    // The first tile's tap loads go out before the weight operand is built.
-    float xv[kStemTcK];
-    stem_gather<C>(a, stem_pixel(a, tile, warp, lane), xv);
-    for (int o = tid; o < kStemTcM; o += kStemTcThreads) {
-        if (o < kStemMaxOC) sBias[o] = (a.b && o < a.OC) ? __ldg(a.b + o) : 0.0f;
-        float wv[kStemTcK];
+    // Global memory from here on; the group's first loads go out before the
+    // weight operand is built.
+    pdl_wait();
+    if (gtid == 0) {
+        if (TMA) {
+            for (int k = 0; k < 2; ++k)
+                if (tile + k * tstep < tend) {
+                    stem_load_halo(&tmX, a, tile + k * tstep, sHalo + (uint32_t)k * a.halo_bytes, barH + 8u * k);
+                    halo_pending[k] = 1u;
+                }
+        }
+    }
+    if (!TMA) {
+        px = stem_pixel(a, tile * kStemPxM + gtid);
+        if (active) stem_gather<C>(a, px, xv);
+    }
+    for (int o = tid; o < a.ocp; o += blockDim.x) sBias[o] = (a.b && o < a.OC) ? __ldg(a.b + o) : 0.0f;
+    for (int r = tid; r < nrows; r += blockDim.x) {
+        const bool lo_part = r >= a.ocp;
+        const int oc = lo_part ? r - a.ocp : r;
+        float v[KP];
 #pragma unroll
-        for (int q = 0; q < kStemTcK; ++q)
-            wv[q] = (o < a.OC && q < KT) ? __ldg(a.w + (long long)o * KT + q) : 0.0f;
-        store_split_row(sWh, sWl, o, wv);
+        for (int t = 0; t < T; ++t) {
+            float h, l;
+            tf32_split(oc < a.OC ? __ldg(a.w + (long long)oc * T + t) : 0.0f, h, l);
+            v[t] = v[T + t] = lo_part ? l : h;
+        }
+#pragma unroll
+        for (int t = 2 * T; t < KP; ++t) v[t] = 0.0f;
+        store_operand_row<KP>(sB, bchunk, r, v);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const int q4 = warp & 3;                     // TMEM lane quadrant: channels 32*q4 ..
-    const int gh = warp >> 2;                    // pixel groups 4*gh .. 4*gh+3 in the epilogue
-    const bool epi_warp = 32 * q4 < a.OC;
-    // Staging tiles: epilogue warp e = gh * nq + q4 owns tiles [e*nbuf, e*nbuf + nbuf).
-    const int nq = (a.OC + 31) / 32, nepi = 2 * nq;
-    const int nbuf = nepi <= 2 ? 4 : (nepi <= 4 ? 2 : 1);
-    const uint32_t ys0 = sY + 4096u * (uint32_t)((gh * nq + q4) * nbuf);
-    int slot = 0;
+    // This group's accumulator: its share of the columns, lanes of quadrant q.
+    const uint32_t tacc = *tmem_slot + (uint32_t)g * (a.tmem_cols / (uint32_t)G);
+    const uint32_t tlane = tacc + ((uint32_t)(q * 32) << 16);
 
-    long long prev = -1;                         // tile whose epilogue is pending
-    int i = 0;
-    for (;; ++i) {
-        const bool have = tile < a.tiles;
-        const int bsel = i & 1;
-        if (have) {
-            // Pixel operands of this tile; buffer bsel was last read by the
-            // MMAs of tile i-2, which every thread saw complete (iteration i-1).
-            const uint32_t ph = sP + 65536u * bsel, pl = ph + 32768u;
-            store_split_row(ph, pl, tid, xv);
+    uint32_t mphase = 0;
+    bool any = false;
+    if (TMA) {
+        const int r = gtid / kStemTileW, j = gtid % kStemTileW;    // this thread's pixel in the tile
+        const int s = a.stride;
+        const bool pair_taps = s == 2 && (a.hd & 1) && (a.hbw % 2 == 0);
+        for (int k = 0; active; ++k) {
+            const int hb = k & 1;
+            const uint32_t hbuf = sHalo + (uint32_t)hb * a.halo_bytes;
+            const bool landed = warp_wait(barH + 8u * hb, (uint32_t)((k >> 1) & 1), a.wait_limit_cycles);
+            if (gtid == 0 && landed) halo_pending[hb] = 0;
+            {
+                const float *h = reinterpret_cast<const float *>(smem_raw + (hbuf - raw));
+                if (pair_taps) {
+                    // Stride 2, odd hd: taps 1 and 2 of a row sit at an even
+                    // column, so one 8-byte load fetches both.
+#pragma unroll
+                    for (int c = 0; c < C; ++c)
+#pragma unroll
+                        for (int ky = 0; ky < 3; ++ky) {
+                            const float *hr = h + (c * a.hbh + r * 2 + ky) * a.hbw + j * 2 + a.hd;
+                            const float2 t12 = *reinterpret_cast<const float2 *>(hr + 1);
+                            xv[(c * 3 + ky) * 3] = hr[0];
+                            xv[(c * 3 + ky) * 3 + 1] = t12.x;
+                            xv[(c * 3 + ky) * 3 + 2] = t12.y;
+                        }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C; ++c)
+#pragma unroll
+                        for (int ky = 0; ky < 3; ++ky) {
+                            const float *hr = h + (c * a.hbh + r * s + ky) * a.hbw + j * s + a.hd;
+#pragma unroll
+                            for (int kx = 0; kx < 3; ++kx) xv[(c * 3 + ky) * 3 + kx] = hr[kx];
+                        }
+                }
+            }
+            // The previous tile's output stores have read the region.
+            if (gtid == 0) bulk_wait_read<0>();
+            named_barrier(1 + g, kStemPxThreads);          // halo buffer hb read by every thread
+            const long long ahead = tile + 2 * tstep;
+            if (gtid == 0 && ahead < tend) {
+                stem_load_halo(&tmX, a, ahead, hbuf, barH + 8u * hb);
+                halo_pending[hb] = 1u + (uint32_t)(((k + 2) >> 1) & 1);
+            }
+            store_pixel_row<C>(sA, gtid, xv);
             fence_proxy_async_shared();
             tc_fence_before();
-            __syncthreads();
+            named_barrier(1 + g, kStemPxThreads);
             tc_fence_after();
-            if (tid == 0) {
-                const uint64_t wh = sw128_kmajor_desc(sWh), wl = sw128_kmajor_desc(sWl);
-                const uint64_t xh = sw128_kmajor_desc(ph), xl = sw128_kmajor_desc(pl);
-                const uint32_t d = tmem + (uint32_t)(bsel * kStemTcPx);
-                // K-steps of 8 tf32 = 32 bytes = descriptor start + 2. Small
-                // cross terms first, the hi x hi term last.
-#pragma unroll
-                for (int kk = 0; kk < kStemTcK / 8; ++kk) tc_mma_tf32(d, wh + 2u * kk, xl + 2u * kk, a.idesc, kk);
-#pragma unroll
-                for (int kk = 0; kk < kStemTcK / 8; ++kk) tc_mma_tf32(d, wl + 2u * kk, xh + 2u * kk, a.idesc, 1);
-#pragma unroll
-                for (int kk = 0; kk < kStemTcK / 8; ++kk) tc_mma_tf32(d, wh + 2u * kk, xh + 2u * kk, a.idesc, 1);
-                tc_commit(sBar + 8u * bsel);
+            if (gtid == 0) {
+                stem_mmas<KP>(tacc, sA, sB, bchunk, a.idesc);
+                tc_commit(barM);
             }
-            // The next tile's taps load while the tensor core works.
-            if (tile + tstep < a.tiles) stem_gather<C>(a, stem_pixel(a, tile + tstep, warp, lane), xv);
-        }
-        if (prev >= 0) {
-            // Epilogue of tile `prev` (buffer (i-1)&1): every warp sees its
-            // MMAs complete (which also frees that pixel buffer).
-            const int pb = (i - 1) & 1;
-            int ok = 1;
-            if (lane == 0) ok = wait_bounded(sBar + 8u * pb, (uint32_t)(((i - 1) >> 1) & 1), a.wait_limit_cycles, nullptr);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok && lane == 0) atomicOr(&g_device_error, 1u);
+            any = true;
+            warp_wait(barM, mphase, a.wait_limit_cycles);
+            mphase ^= 1u;
             tc_fence_after();
-            if (epi_warp) {
-                const int oc = 32 * q4 + lane;
-                const float bias = sBias[oc];
+            // Staging tile [oc][row][pixel] in the region (the MMAs are done with it).
+            const uint32_t stg = sA + (uint32_t)((r * kStemTileW + j) * 4);
 #pragma unroll 1
-                for (int gg = 0; gg < 4; ++gg) {
-                    const int grp = 4 * gh + gg;
-                    const StemPix p = stem_pixel(a, prev, grp, 0);
-                    if (!p.group_ok) continue;
-                    uint32_t v[32];
-                    tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(pb * kStemTcPx + grp * 32), v);
-                    tmem_ld_wait();
-                    if (a.tma_store) {
-                        const uint32_t ys = ys0 + 4096u * (uint32_t)slot;
-                        if (++slot == nbuf) slot = 0;
-                        // The store that last used this staging tile has read it.
-                        if (lane == 0) {
-                            if (nbuf == 4) bulk_wait_read<3>();
-                            else if (nbuf == 2) bulk_wait_read<1>();
-                            else bulk_wait_read<0>();
-                        }
-                        __syncwarp();
-                        // Row `lane` (= channel) of a [32 ch][32 px] block, 128-byte swizzle.
+            for (int c0 = 0; c0 < a.ocp; c0 += 16) {
+                uint32_t hv[16], lv[16];
+                tmem_ld16(tlane + (uint32_t)c0, hv);
+                tmem_ld16(tlane + (uint32_t)(a.ocp + c0), lv);
+                tmem_ld_wait();
+                float bias[16];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            float r[4];
+                for (int e4 = 0; e4 < 4; ++e4)
+                    *reinterpret_cast<float4 *>(&bias[4 * e4]) = reinterpret_cast<const float4 *>(sBias + c0)[e4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                r[e] = epilogue(__uint_as_float(v[4 * j + e]), bias, a.relu);
-                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                             ys + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) << 4)),
-                                         "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3])
-                                         : "memory");
-                        }
-                        fence_proxy_async_shared();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_4d(&tmY, ys, p.ow0, p.oh, 32 * q4, p.n);
-                            bulk_commit_group();
-                        }
-                    } else if (oc < a.OC) {
-                        const long long plane = (long long)a.OH * a.OW;
-                        float *yp = a.y + ((long long)p.n * a.OC + oc) * plane + (long long)p.oh * a.OW + p.ow0;
+                for (int e = 0; e < 16; ++e) {
+                    const int oc = c0 + e;
+                    const float v = epilogue(__uint_as_float(hv[e]) + __uint_as_float(lv[e]), bias[e], a.relu);
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + (uint32_t)(oc * kStemTileR * kStemTileW * 4)),
+                                 "f"(v)
+                                 : "memory");
+                }
+            }
+            fence_proxy_async_shared();
+            tc_fence_before();
+            named_barrier(1 + g, kStemPxThreads);
+            if (gtid == 0) {
+                const StemTile st = stem_tile(a, tile);
+                const uint32_t box_bytes = (uint32_t)(a.ybox_c * kStemTileR * kStemTileW * 4);
+                for (int c0 = 0, bi = 0; c0 < a.OC; c0 += a.ybox_c, ++bi)
+                    tma_store_4d(&tmY, sA + (uint32_t)bi * box_bytes, st.ow0, st.oh0, c0, st.n);
+                bulk_commit_group();
+            }
+            tile += tstep;
+            if (tile >= tend) break;
+        }
+        if (gtid == 0) {
+            bulk_wait_all();
+            // A halo wait that ran out leaves its load possibly in flight:
+            // wait for that buffer's barrier to complete a phase (bounded).
+            for (int k = 0; k < 2; ++k)
+                if (halo_pending[k]) wait_bounded(barH + 8u * k, halo_pending[k] - 1u, a.wait_limit_cycles, nullptr);
+        }
+    } else {
+        while (active) {
+            // The previous tile's MMAs, which read the operand, completed
+            // before every thread of the group left its wait below.
+            store_pixel_row<C>(sA, gtid, xv);
+            fence_proxy_async_shared();
+            tc_fence_before();
+            named_barrier(1 + g, kStemPxThreads);
+            tc_fence_after();
+            if (gtid == 0) {
+                stem_mmas<KP>(tacc, sA, sB, bchunk, a.idesc);
+                tc_commit(barM);
+            }
+            any = true;
+            const StemPixel cur = px;
+            const long long next = tile + tstep;
+            if (next < tend) {
+                px = stem_pixel(a, next * kStemPxM + gtid);
+                stem_gather<C>(a, px, xv);                 // in flight during the wait and the stores
+            }
+            warp_wait(barM, mphase, a.wait_limit_cycles);
+            mphase ^= 1u;
+            tc_fence_after();
+            float *yp = a.y + cur.n * a.OC * a.ohw + cur.rem;
+#pragma unroll 1
+            for (int c0 = 0; c0 < a.ocp; c0 += 16) {
+                uint32_t hv[16], lv[16];
+                tmem_ld16(tlane + (uint32_t)c0, hv);
+                tmem_ld16(tlane + (uint32_t)(a.ocp + c0), lv);
+                tmem_ld_wait();
+                if (cur.valid) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (p.ow0 + e < a.OW) yp[e] = epilogue(__uint_as_float(v[e]), bias, a.relu);
+                    for (int e = 0; e < 16; ++e) {
+                        const int oc = c0 + e;
+                        if (oc < a.OC)
+                            yp[(long long)oc * a.ohw] =
+                                epilogue(__uint_as_float(hv[e]) + __uint_as_float(lv[e]), sBias[oc], a.relu);
                     }
                 }
             }
-            tc_fence_before();                   // accumulator pb is rewritten two tiles on
+            // TMEM reads complete before the group barrier that precedes the next MMAs.
+            tc_fence_before();
+            if (next >= tend) break;
+            tile = next;
         }
-        if (!have) break;
-        prev = tile;
-        tile += tstep;
     }
-    if (lane == 0) bulk_wait_all();
-
+    // A wait that ran out leaves its MMAs possibly in flight: wait once more
+    // (bounded) for the group's last commit before the TMEM is released.
+    if (any && gtid == 0) wait_bounded(barM, mphase ^ 1u, a.wait_limit_cycles, nullptr);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (tid < 32) {
         tc_fence_after();
-        tmem_dealloc(tmem, a.tmem_cols);
+        tmem_dealloc(*tmem_slot, a.tmem_cols);
     }
 }
 
-size_t stem_tc_smem_bytes() {
-    return 1024 + 32768 + 2 * 65536 + 4096 * (kStemTcThreads / 32) + 16 + 16 + 4 * kStemMaxOC;
+inline uint32_t align1k(size_t v) { return (uint32_t)((v + 1023) & ~size_t(1023)); }
+
+inline size_t stem_tc_smem_bytes(const StemTcArgs &a, int C, bool tma, int groups) {
+    const int KP = (2 * C * 9 + 7) / 8 * 8, KCH = (KP + 31) / 32;
+    return 1024 + (size_t)KCH * 2 * a.ocp * 128 + (size_t)groups * a.region_bytes +
+           (tma ? 2 * (size_t)groups * a.halo_bytes : 0) + 24 * (size_t)groups + 32 + 4 * (size_t)a.ocp;
 }
 
 template <int C>
@@ -301,39 +461,75 @@ cudaError_t launch_stem_tf32_c(const Problem &p, const float *x, const float *w,
     StemTcArgs a{};
     a.x = x; a.w = w; a.b = b; a.y = y;
     a.H = p.H; a.W = p.W; a.OC = p.OC; a.OH = p.OH; a.OW = p.OW; a.pad = p.pad; a.stride = p.stride;
-    a.groups_w = (p.OW + 31) / 32;
-    a.groups = (long long)p.N * p.OH * a.groups_w;
-    a.tiles = (a.groups + 7) / 8;
-    a.idesc = make_idesc_tf32(kStemTcM, kStemTcPx);
-    a.tmem_cols = 512;                           // two 256-column accumulators
+    a.ocp = (p.OC + 15) / 16 * 16;
+    a.ohw = (long long)p.OH * p.OW;
+    a.npix = (long long)p.N * a.ohw;
+    a.idesc = make_idesc_tf32(kStemPxM, 2 * a.ocp);
+    uint32_t cols = 32;                          // one group's accumulator
+    while (cols < (uint32_t)(2 * a.ocp)) cols *= 2;
     a.relu = p.act == GBCONV_ACT_RELU;
     const double cyc = (double)wait_limit_ns() * (double)info.clock_khz * 1e-6;
     a.wait_limit_cycles = cyc > 9.0e18 ? (long long)9e18 : (long long)cyc;
+    const uint32_t operand_bytes = (uint32_t)StemShape<C>::KCH * 16384u;
 
-    alignas(64) CUtensorMap tmY;
+    // TMA input and output: rows and bases 16-byte aligned, halo box within 256 columns.
+    alignas(64) CUtensorMap tmX, tmY;
+    std::memset(&tmX, 0, sizeof(tmX));
     std::memset(&tmY, 0, sizeof(tmY));
-    a.tma_store = (p.OW % 4 == 0) && ((uintptr_t)y % 16 == 0);
-    if (a.tma_store) {
+    bool tma = p.W % 4 == 0 && p.OW % 4 == 0 && (uintptr_t)x % 16 == 0 && (uintptr_t)y % 16 == 0 &&
+               p.stride <= kStemMaxTmaStride;
+    if (tma) {
+        a.hd = ((-p.pad) % 4 + 4) % 4;
+        a.hbw = (a.hd + (kStemTileW - 1) * p.stride + 3 + 3) / 4 * 4;   // >= hd + 63 s + 3, a multiple of 4
+        a.hbh = (kStemTileR - 1) * p.stride + 3;
+        a.halo_box_bytes = (uint32_t)(C * a.hbh * a.hbw * 4);
+        a.halo_bytes = align1k(a.halo_box_bytes);
+        a.ybox_c = a.ocp < 32 ? a.ocp : 32;
+        // Output boxes cover roundup(OCP, ybox_c) staged channels.
+        const int staged_c = (a.ocp + a.ybox_c - 1) / a.ybox_c * a.ybox_c;
+        const uint32_t stage_bytes = (uint32_t)(staged_c * kStemTileR * kStemTileW * 4);
+        a.region_bytes = align1k(operand_bytes > stage_bytes ? operand_bytes : stage_bytes);
+        a.tiles_w = (p.OW + kStemTileW - 1) / kStemTileW;
+        a.tiles_h = (p.OH + kStemTileR - 1) / kStemTileR;
+        a.tiles = (long long)p.N * a.tiles_h * a.tiles_w;
         PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
-        // y as {OW, OH, OC, N}; a box is 32 pixels of one row x 32 channels,
-        // staged with the 128-byte swizzle.
-        const cuuint64_t dims[4] = {(cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.OC, (cuuint64_t)p.N};
-        const cuuint64_t row = (cuuint64_t)p.OW * 4;
-        const cuuint64_t strides[3] = {row, row * p.OH, row * p.OH * p.OC};
-        const cuuint32_t box[4] = {32, 1, 32, 1};
         const cuuint32_t es[4] = {1, 1, 1, 1};
-        if (!encode || encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, dims, strides, box, es,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            a.tma_store = 0;
+        // x as {W, H, C, N}; a box is the halo of one tile.
+        const cuuint64_t xd[4] = {(cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)C, (cuuint64_t)p.N};
+        const cuuint64_t xr = (cuuint64_t)p.W * 4;
+        const cuuint64_t xs[3] = {xr, xr * p.H, xr * p.H * C};
+        const cuuint32_t xb[4] = {(cuuint32_t)a.hbw, (cuuint32_t)a.hbh, (cuuint32_t)C, 1};
+        // y as {OW, OH, OC, N}; a box is 64 pixels x 2 rows x ybox_c channels.
+        const cuuint64_t yd[4] = {(cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.OC, (cuuint64_t)p.N};
+        const cuuint64_t yr = (cuuint64_t)p.OW * 4;
+        const cuuint64_t ys[3] = {yr, yr * p.OH, yr * p.OH * p.OC};
+        const cuuint32_t yb[4] = {(cuuint32_t)kStemTileW, (cuuint32_t)kStemTileR, (cuuint32_t)a.ybox_c, 1};
+        tma = encode &&
+              encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), xd, xs, xb, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+              encode(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, y, yd, ys, yb, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
-    const size_t smem = stem_tc_smem_bytes();
-    auto kern = stem_tf32_kernel<C>;
+    if (!tma) {
+        a.halo_box_bytes = a.halo_bytes = 0;
+        a.region_bytes = operand_bytes;
+        a.tiles = (a.npix + kStemPxM - 1) / kStemPxM;
+    }
+
+    // Groups per CTA: as many (1, 2 or 4) as shared memory and the SM's 512
+    // TMEM columns allow.
+    int G = kStemMaxGroups;
+    while (G > 1 && (stem_tc_smem_bytes(a, C, tma, G) > kStemSmemLimit || (uint32_t)G * cols > 512u)) G /= 2;
+    a.groups = G;
+    a.tmem_cols = cols * (uint32_t)G;
+    const size_t smem = stem_tc_smem_bytes(a, C, tma, G);
+    auto kern = tma ? stem_tf32_kernel<C, true> : stem_tf32_kernel<C, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    // One persistent CTA per SM.
-    const long long grid = a.tiles < info.sms ? a.tiles : info.sms;
-    kern<<<(unsigned)grid, kStemTcThreads, smem, s>>>(tmY, a);
-    return cudaGetLastError();
+    // One CTA per SM (a kernel that uses TMEM is resident once per SM).
+    const long long ctas = (a.tiles + G - 1) / G;
+    const long long grid = ctas < info.sms ? ctas : info.sms;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kStemPxThreads * G), smem, s, tmX, tmY, a);
 }

@@ -95,9 +95,10 @@ typedef enum gbconv_algo {
     GBCONV_ALGO_DIRECT = 1,      /* direct, shared-memory halo + register micro-tile (small IC*k^d) */
     GBCONV_ALGO_IGEMM_FFMA = 2,  /* implicit GEMM on CUDA cores, exact fp32 FMA */
     GBCONV_ALGO_IGEMM_TC = 3,    /* implicit GEMM on tcgen05 tensor cores (fp16/bf16 storage) */
-    GBCONV_ALGO_DIRECT_TC = 4    /* fp32, 2D, k = 3, C <= 3 (image stems) on tcgen05 tensor cores: each
-                                    fp32 product as three TF32 products (x_hi*w_lo + x_lo*w_hi +
-                                    x_hi*w_hi), fp32 accumulate; relative error near 2^-20 per product */
+    GBCONV_ALGO_DIRECT_TC = 4    /* fp32, 2D, k = 3, C <= 4, OC <= 128 (image stems) on tcgen05 tensor
+                                    cores: x and w split into TF32 hi + lo parts, one MMA chain forms
+                                    (x_hi + x_lo) * w_hi and (x_hi + x_lo) * w_lo, fp32 accumulate;
+                                    relative error near 2^-20 per product */
 } gbconv_algo;
 
 /*

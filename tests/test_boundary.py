@@ -81,7 +81,7 @@ BAD = [
     (dict(N=4096, C=4096, H=4096, W=4096), gb.ERR_SHAPE),
     (dict(dtype=3), gb.ERR_DTYPE), (dict(dtype=-1), gb.ERR_DTYPE),
     (dict(act=2), gb.ERR_ACT), (dict(act=-7), gb.ERR_ACT),
-    (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, C=4), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, OC=129), gb.ERR_ALGO),
+    (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, C=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, OC=129), gb.ERR_ALGO),
     (dict(flags=8), gb.ERR_RESERVED), (dict(flags=3), gb.ERR_RESERVED),
     (dict(tpad=gb.TPAD_CAUSAL), gb.ERR_SHAPE),      # conv2d: symmetric frames only
     (dict(algo=gb.ALGO_IGEMM_TC), gb.ERR_ALGO),     # tensor cores need 16-bit
@@ -157,19 +157,23 @@ def test_shapes_and_algorithm_of_the_five_layers(idx):
     assert (od, oh, ow) == L.out_dims()
     st, algo = gb.select_algo(d, L.ndim)
     assert st == gb.OK
-    expect = {1: gb.ALGO_DIRECT, 2: gb.ALGO_DIRECT, 3: gb.ALGO_IGEMM_FFMA,
+    expect = {1: gb.ALGO_DIRECT, 2: gb.ALGO_DIRECT_TC, 3: gb.ALGO_IGEMM_FFMA,
               4: gb.ALGO_IGEMM_TC, 5: gb.ALGO_IGEMM_TC}[idx]
     assert algo == expect, gb.algo_name(algo)
 
 
-def test_auto_picks_tensor_core_stem_for_wide_fp32_stems():
-    """fp32 3x3 stems with 48+ output channels go to the tensor-core stem;
-    narrower ones, other dtypes and C > 3 do not."""
+def test_auto_picks_tensor_core_stem_for_fp32_stems():
+    """fp32 3x3 stems (C <= 4) with 16 to 128 output channels go to the
+    tensor-core stem; narrower and wider ones, other dtypes, C > 4 and the
+    fused pool do not."""
     pick = lambda **kw: gb.select_algo(_desc(**kw), 2)[1]
     assert pick(C=3, OC=64, H=640, W=640, k=3, pad=1, stride=2) == gb.ALGO_DIRECT_TC
     assert pick(C=3, OC=128, H=64, W=64, k=3, pad=1, stride=1) == gb.ALGO_DIRECT_TC
-    assert pick(C=3, OC=32, H=640, W=640, k=3, pad=1, stride=2) == gb.ALGO_DIRECT
-    assert pick(C=4, OC=64, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
+    assert pick(C=3, OC=32, H=640, W=640, k=3, pad=1, stride=2) == gb.ALGO_DIRECT_TC
+    assert pick(C=4, OC=16, H=64, W=64, k=3, pad=1, stride=1) == gb.ALGO_DIRECT_TC
+    assert pick(C=3, OC=8, H=32, W=32, k=3, pad=1, stride=1) == gb.ALGO_DIRECT
+    assert pick(C=5, OC=64, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
+    assert pick(C=3, OC=32, H=64, W=64, k=3, pad=1, stride=2, pool=True) == gb.ALGO_DIRECT
     assert pick(C=3, OC=160, H=64, W=64, k=3, pad=1, stride=1) != gb.ALGO_DIRECT_TC
     assert pick(C=3, OC=64, H=64, W=64, k=3, pad=1, stride=1, dtype=gb.F16) != gb.ALGO_DIRECT_TC
 

@@ -161,6 +161,17 @@ SWEEP = [
     (A_DTC, _L(C=3, H=9, W=9, OC=100, stride=3)),
     (A_DTC, _L(C=3, H=12, W=30, OC=128, relu=True)),
     (A_DTC, _L(C=2, H=1, W=5, OC=3)),
+    (A_DTC, _L(C=4, H=21, W=37, OC=32, stride=2, relu=True)),
+    (A_DTC, _L(N=5, C=3, H=13, W=11, OC=17)),
+    (A_DTC, _L(C=4, H=8, W=8, OC=1, pad=0)),
+    (A_DTC, _L(N=2, C=3, H=100, W=130, OC=32, stride=2, relu=True)),
+    # rows 16-byte aligned: TMA halo loads and tensor stores
+    (A_DTC, _L(C=3, H=64, W=64, OC=32, stride=2, relu=True)),
+    (A_DTC, _L(N=2, C=3, H=50, W=200, OC=24, stride=2)),
+    (A_DTC, _L(C=1, H=30, W=36, OC=128, relu=True)),
+    (A_DTC, _L(C=4, H=20, W=68, OC=48)),
+    (A_DTC, _L(C=2, H=27, W=96, OC=64, stride=3, bias=False)),
+    (A_DTC, _L(N=3, C=3, H=16, W=16, OC=16, stride=2, relu=True)),
     # conv3d frame padding: causal (k-1 zero frames in front) and none, on
     # every kernel family that takes 3D, strides 1 and 2, k 3 and 5
     (A_DIRECT, _L(C=2, D=5, H=7, W=9, OC=6, ndim=3, tpad=CAUSAL)),
