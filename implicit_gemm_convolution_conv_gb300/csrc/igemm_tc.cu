@@ -605,7 +605,8 @@ cudaError_t launch_igemm_tc(const Problem &p, const void *xc, const void *wp, co
 }
 
 bool stem_tc_supported(const Problem &p) {
-    return p.ndim == 2 && p.dtype == GBCONV_F32 && p.k == 3 && p.C <= kStemMaxC && p.OC <= kStemMaxOC;
+    return p.ndim == 2 && p.dtype == GBCONV_F32 && p.k == 3 && p.C <= kStemMaxC && p.OC <= kStemMaxOC &&
+           (int64_t)p.N * p.OH * p.OW <= kStemMaxPixels;
 }
 
 cudaError_t launch_stem_tc(const Problem &p, const void *x, const void *w, const float *b, void *y,
