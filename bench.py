@@ -41,9 +41,13 @@ METRIC = ("conv TFLOP/s and % of roofline per layer shape at 1 GB300 "
 WORKLOADS = {"detection_stem": 2, "tiny": 1, "text_line_batch": 3,
              "wide_dense_f16": 4, "video_vae_conv3d_f16": 5}
 # Variants of a layer shape: (layer, fields changed, name suffix). The fused
-# 2x2 max pool of the stem, and the video-VAE conv3d with causal frame padding.
+# 2x2 max pool of the stem, the video-VAE conv3d with causal frame padding,
+# and the two tensor-core layers with channels-last activations (x read in
+# place, no layout pass: the layer-chaining case).
 VARIANTS = {"detection_stem_maxpool": (2, {"pool": True}, "+maxpool2x2"),
-            "video_vae_conv3d_f16_causal": (5, {"tpad": 1}, "+causal_frames")}
+            "video_vae_conv3d_f16_causal": (5, {"tpad": 1}, "+causal_frames"),
+            "wide_dense_f16_channels_last": (4, {"cl": True}, "+channels_last"),
+            "video_vae_conv3d_f16_channels_last": (5, {"cl": True}, "+channels_last")}
 
 
 def workload_layer(name):
@@ -53,6 +57,11 @@ def workload_layer(name):
     base = synthetic.LAYERS[idx]
     return dataclasses.replace(base, name=base.name + suffix, **kw)
 DEFAULT_WORKLOAD = "detection_stem"
+
+
+def device_x(L, inp):
+    """x as the call takes it: NC(D)HW, or channels-last for a `cl` layer."""
+    return np.ascontiguousarray(np.moveaxis(inp.x, 1, -1)) if L.cl else inp.x
 FLUSH_BYTES = 256 << 20
 SM_COUNT_FALLBACK = 152
 FP32_LANES_PER_SM = 128
@@ -248,11 +257,11 @@ def run_ours(args):
 
     L = workload_layer(args.workload)
     inp = synthetic.make_inputs(L)
-    x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
+    x, w = to_device(device_x(L, inp), L.dtype, dev), to_device(inp.w, L.dtype, dev)
     b = torch.from_numpy(inp.b).to(dev)
-    conv = Conv(x, w, b, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool)
+    conv = Conv(x, w, b, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool, channels_last=L.cl)
     launches = {gb.ALGO_DIRECT: 1, gb.ALGO_DIRECT_TC: 1, gb.ALGO_IGEMM_FFMA: 2,
-                gb.ALGO_IGEMM_TC: 3}[conv.algo]
+                gb.ALGO_IGEMM_TC: 2 if L.cl else 3}[conv.algo]
     rot = Rotation(torch, conv)
 
     # warm-up, then exactly K timed steps between barriers
@@ -316,7 +325,8 @@ def run_ours(args):
         roof["kernel"] = kernel
         roof["timed"] = ("one call = one launch" if launches == 1 else
                          f"one call = {launches} launches (weight pack, "
-                         "layout pass, GEMM); times are per call")
+                         + ("" if L.cl or conv.algo != gb.ALGO_IGEMM_TC else "layout pass, ")
+                         + "GEMM); times are per call")
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -343,7 +353,7 @@ def run_ours(args):
     if rank == 0:
         # end to end: pinned host buffers, H2D of x, w, b and D2H of y inside
         # the timed region, through the same C-ABI call
-        hx = torch.from_numpy(np.ascontiguousarray(inp.x)).pin_memory()
+        hx = torch.from_numpy(np.ascontiguousarray(device_x(L, inp))).pin_memory()
         hw = torch.from_numpy(np.ascontiguousarray(inp.w)).pin_memory()
         hb = torch.from_numpy(inp.b).pin_memory()
         hy = torch.empty(conv.y.shape, dtype=conv.y.dtype).pin_memory()
@@ -394,7 +404,7 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
         (VARIANTS[v][0], workload_layer(v)) for v in sorted(VARIANTS)]
     for idx, L in layers:
         inp = synthetic.make_inputs(L)
-        x, w = to_device(inp.x, L.dtype, dev), to_device(inp.w, L.dtype, dev)
+        x, w = to_device(device_x(L, inp), L.dtype, dev), to_device(inp.w, L.dtype, dev)
         b = torch.from_numpy(inp.b).to(dev)
         rec = {"layer": L.name, "flop": L.flops(),
                "bytes": L.compulsory_bytes()}
@@ -404,7 +414,8 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
         t_ideal = max(t_c, t_m)
         t_ideal_335 = max(t_c, L.compulsory_bytes() / 3.35e12)
         for prepack in (False, True):
-            conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack, tpad=L.tpad, pool=L.pool)
+            conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack, tpad=L.tpad, pool=L.pool,
+                        channels_last=L.cl)
             rot = Rotation(torch, conv)
             calls = 200 if idx <= 3 else (100 if idx == 4 else 40)
             for _ in range(3):

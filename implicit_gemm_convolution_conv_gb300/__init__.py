@@ -20,6 +20,7 @@ ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALGO = 7, 8, 9, 10
 ERR_LAYOUT, ERR_OVERLAP, ERR_CUDA, ERR_RESERVED = 11, 12, 13, 14
 TPAD_SYMMETRIC, TPAD_CAUSAL, TPAD_NONE = 0, 1, 2
 FLAG_MAXPOOL2 = 4
+FLAG_CHANNELS_LAST = 8
 ERR_TOO_LARGE = 15
 NOALLOC_SCRATCH_BYTES = 8 << 20
 F32, F16, BF16 = 0, 1, 2
@@ -107,14 +108,16 @@ def _stream(s):
 
 def make_desc(N, C, H, W, OC, k, pad=0, stride=1, D=1, dtype=F32,
               act=ACT_NONE, w_layout=W_OIHW, algo=ALGO_AUTO, workspace=None,
-              workspace_bytes=0, flags=0, tpad=0, pool=False):
+              workspace_bytes=0, flags=0, tpad=0, pool=False,
+              channels_last=False):
     if isinstance(dtype, str):
         dtype = DTYPES[dtype]
     d = Desc()
     d.N, d.C, d.D, d.H, d.W = N, C, D, H, W
     d.OC, d.k, d.pad, d.stride = OC, k, pad, stride
     d.dtype, d.act, d.w_layout, d.algo = dtype, act, w_layout, algo
-    d.flags = flags | tpad | (FLAG_MAXPOOL2 if pool else 0)
+    d.flags = (flags | tpad | (FLAG_MAXPOOL2 if pool else 0) |
+               (FLAG_CHANNELS_LAST if channels_last else 0))
     d.workspace = _ptr(workspace)
     d.workspace_bytes = workspace_bytes
     return d

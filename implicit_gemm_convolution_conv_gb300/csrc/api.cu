@@ -24,7 +24,9 @@ bool in_range(int v, int lo, int hi) { return v >= lo && v <= hi; }
 gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (!d) return GBCONV_ERR_NULL;
     if (ndim != 2 && ndim != 3) return GBCONV_ERR_SHAPE;
-    if ((d->flags & ~(GBCONV_FLAG_TPAD_MASK | GBCONV_FLAG_MAXPOOL2)) != 0) return GBCONV_ERR_RESERVED;
+    if ((d->flags & ~(GBCONV_FLAG_TPAD_MASK | GBCONV_FLAG_MAXPOOL2 | GBCONV_FLAG_CHANNELS_LAST)) != 0)
+        return GBCONV_ERR_RESERVED;
+    const int cl = (d->flags & GBCONV_FLAG_CHANNELS_LAST) ? 1 : 0;
     const int pool = (d->flags & GBCONV_FLAG_MAXPOOL2) ? 1 : 0;
     if (pool && ndim != 2) return GBCONV_ERR_SHAPE;
     const int tpad = d->flags & GBCONV_FLAG_TPAD_MASK;
@@ -65,6 +67,7 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     q.in_vol = (int64_t)q.D * q.H * q.W;
     q.out_vol = od * oh * ow;
     q.pool = pool;
+    q.cl = cl;
     q.YH = pool ? q.OH / 2 : q.OH;
     q.YW = pool ? q.OW / 2 : q.OW;
     if (q.YH <= 0 || q.YW <= 0) return GBCONV_ERR_SHAPE;
@@ -81,7 +84,11 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     // work: the direct kernel. Otherwise an implicit GEMM: tensor cores for
     // 16-bit storage, exact fp32 FMA on CUDA cores for fp32.
     int algo = d->algo;
-    if (algo == GBCONV_ALGO_AUTO) {
+    if (algo == GBCONV_ALGO_AUTO && q.cl) {
+        // Channels-last: the implicit GEMMs only (the direct kernels read NCHW).
+        algo = (q.dtype != GBCONV_F32 && tc_cl_direct(q) && tc_supported(q)) ? GBCONV_ALGO_IGEMM_TC
+                                                                             : GBCONV_ALGO_IGEMM_FFMA;
+    } else if (algo == GBCONV_ALGO_AUTO) {
         // fp32 3x3 stems of 16+ output channels: the tensor-core stem
         // (measured faster than the CUDA-core stem from 16 to 128 channels
         // on 640 x 640 images, stride 1 and 2).
@@ -101,6 +108,8 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (algo == GBCONV_ALGO_IGEMM_TC && (q.dtype == GBCONV_F32 || !tc_supported(q)))
         return GBCONV_ERR_ALGO;
     if (algo == GBCONV_ALGO_DIRECT_TC && !stem_tc_supported(q)) return GBCONV_ERR_ALGO;
+    if (q.cl && !(algo == GBCONV_ALGO_IGEMM_FFMA || (algo == GBCONV_ALGO_IGEMM_TC && tc_cl_direct(q))))
+        return GBCONV_ERR_ALGO;
     // The fused pool lives in the few-channel 3x3 direct kernel only.
     if (q.pool && !(algo == GBCONV_ALGO_DIRECT && stem_supported(q))) return GBCONV_ERR_ALGO;
     *p = q;
@@ -134,6 +143,8 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
         (b && !aligned(b, 4)))
         return GBCONV_ERR_ALIGN;
     if (p.w_layout == GBCONV_W_PACKED && !aligned(w, 256)) return GBCONV_ERR_ALIGN;
+    // The tensor-core kernel reads channels-last x in place with TMA.
+    if (p.algo == GBCONV_ALGO_IGEMM_TC && p.cl && !aligned(x, 16)) return GBCONV_ERR_ALIGN;
     const size_t xb = (size_t)p.x_elems * p.elt, yb = (size_t)p.y_elems * p.elt;
     const size_t wb = p.w_layout == GBCONV_W_PACKED ? packed_weight_bytes(p)
                                                     : (size_t)p.w_elems * p.elt;
@@ -175,8 +186,12 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
             e = launch_pack_tc(p, w, wsp + ws.w_off, s);
             wp = wsp + ws.w_off;
         }
-        if (e == cudaSuccess) e = launch_to_channels_last(p, x, wsp + ws.x_off, s);
-        if (e == cudaSuccess) e = launch_igemm_tc(p, wsp + ws.x_off, wp, b, y, s);
+        if (p.cl) {
+            if (e == cudaSuccess) e = launch_igemm_tc(p, x, wp, b, y, s);
+        } else {
+            if (e == cudaSuccess) e = launch_to_channels_last(p, x, wsp + ws.x_off, s);
+            if (e == cudaSuccess) e = launch_igemm_tc(p, wsp + ws.x_off, wp, b, y, s);
+        }
         break;
     }
     default:
@@ -212,7 +227,7 @@ size_t packed_weight_bytes(const Problem &p) {
 Workspace workspace_layout(const Problem &p) {
     Workspace ws;
     size_t off = 0;
-    if (p.algo == GBCONV_ALGO_IGEMM_TC) {
+    if (p.algo == GBCONV_ALGO_IGEMM_TC && !p.cl) {
         ws.x_off = off;
         ws.x_bytes = (size_t)p.N * p.in_vol * tc_cpad(p.C) * p.elt;
         off = align256(off + ws.x_bytes);

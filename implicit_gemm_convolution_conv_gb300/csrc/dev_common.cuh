@@ -15,11 +15,15 @@ template <> struct Storage<float> {
     static __device__ __forceinline__ float from_float(float v) { return v; }
 };
 template <> struct Storage<__half> {
+    using Pair = __half2;
+    static __device__ __forceinline__ Pair pack2(float lo, float hi) { return __floats2half2_rn(lo, hi); }
     static __device__ __forceinline__ float load(const __half *p) { return __half2float(__ldg(p)); }
     static __device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
     static __device__ __forceinline__ __half from_float(float v) { return __float2half_rn(v); }
 };
 template <> struct Storage<__nv_bfloat16> {
+    using Pair = __nv_bfloat162;
+    static __device__ __forceinline__ Pair pack2(float lo, float hi) { return __floats2bfloat162_rn(lo, hi); }
     static __device__ __forceinline__ float load(const __nv_bfloat16 *p) { return __bfloat162float(__ldg(p)); }
     static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
     static __device__ __forceinline__ __nv_bfloat16 from_float(float v) { return __float2bfloat16_rn(v); }

@@ -7,7 +7,10 @@
 //   B[kk][oc] = packed weights, row kk = tap * IC + ic,
 //   y[n][oc][pixel] = epilogue(sum_kk A[m][kk] * B[kk][oc]).
 // A is never materialised (no im2col buffer): each CTA gathers its A tile
-// straight from the NCHW/NCDHW input into shared memory. CTA tile BM x BN,
+// straight from the input into shared memory. The generic kernel takes the
+// input and output element strides as arguments, so it reads and writes both
+// NC(D)HW and channels-last N(D)HWC tensors; the packed-FMA variant below is
+// NC(D)HW only. CTA tile BM x BN,
 // K step BK, two shared-memory stages with the next stage prefetched into
 // registers while the current one is multiplied; each thread accumulates an
 // 8 x 8 register tile (two 4-wide pixel groups x two 4-wide channel groups).
@@ -31,6 +34,11 @@ struct FfmaArgs {
     int64_t M, out_vol, in_hw;
     int K;              // taps * C
     int relu;
+    // Element strides (generic kernel): x offset = n * xs_n + c * xs_c +
+    // id * xs_d + ih * xs_h + iw * xs_w; y offset = n * ys_n + oc * ys_c +
+    // pixel * ys_p, pixel = (od * OH + oh) * OW + ow.
+    int64_t xs_n, xs_c, xs_d, xs_h, xs_w;
+    int64_t ys_n, ys_c, ys_p;
 };
 
 template <typename T>
@@ -56,8 +64,7 @@ __global__ void __launch_bounds__(NT) igemm_ffma_kernel(const FfmaArgs a) {
     }
     const int id0 = od * a.stride - a.pad_d, ih0 = oh * a.stride - a.pad,
               iw0 = ow * a.stride - a.pad;
-    const int64_t x_img = (int64_t)img * a.C * a.D * a.in_hw;
-    const int64_t c_stride = (int64_t)a.D * a.in_hw;
+    const T *x_img = x + (int64_t)img * a.xs_n;
 
     // B loader: row tid/8 of the stage, 8 consecutive output channels.
     const int b_row = tid / 8, b_col = (tid % 8) * 8;
@@ -75,8 +82,7 @@ __global__ void __launch_bounds__(NT) igemm_ffma_kernel(const FfmaArgs a) {
                 const int kx = tap % a.k, ky = (tap / a.k) % a.k, kz = tap / (a.k * a.k);
                 const int id = id0 + kz, ih = ih0 + ky, iw = iw0 + kx;
                 if (id >= 0 && id < a.D && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W)
-                    v = Storage<T>::load(x + x_img + c * c_stride + (int64_t)id * a.in_hw +
-                                         (int64_t)ih * a.W + iw);
+                    v = Storage<T>::load(x_img + c * a.xs_c + id * a.xs_d + ih * a.xs_h + iw * a.xs_w);
             }
             a_reg[r] = v;
             if (++c == a.C) { c = 0; ++tap; }
@@ -139,7 +145,7 @@ __global__ void __launch_bounds__(NT) igemm_ffma_kernel(const FfmaArgs a) {
             const int oc = n0 + (j < 4 ? tn * 4 + j : 32 + tn * 4 + (j - 4));
             if (oc >= a.OC) continue;
             const float bias = a.b ? __ldg(a.b + oc) : 0.0f;
-            y[(im * a.OC + oc) * a.out_vol + pix] =
+            y[im * a.ys_n + oc * a.ys_c + pix * a.ys_p] =
                 Storage<T>::from_float(epilogue(acc[i][j], bias, a.relu));
         }
     }
@@ -297,8 +303,8 @@ __global__ void pack_ffma_kernel(const T *__restrict__ w, T *__restrict__ wp,
 }
 
 template <typename T>
-cudaError_t launch_ffma_typed(const FfmaArgs &a, cudaStream_t s) {
-    if (a.C % WBK == 0) {
+cudaError_t launch_ffma_typed(const FfmaArgs &a, bool cl, cudaStream_t s) {
+    if (a.C % WBK == 0 && !cl) {
         auto kern = igemm_ffma2_kernel<T>;
         const int smem = (2 * 2 * WBK * WBM + 2 * WBK * WBN) * (int)sizeof(float);
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -333,10 +339,20 @@ cudaError_t launch_igemm_ffma(const Problem &p, const void *x, const void *wp,
     a.in_hw = (int64_t)p.H * p.W;
     a.K = p.taps * p.C;
     a.relu = p.act == GBCONV_ACT_RELU;
+    const int64_t hw = (int64_t)p.H * p.W;
+    a.xs_n = (int64_t)p.C * p.D * hw;
+    a.ys_n = (int64_t)p.OC * p.out_vol;
+    if (p.cl) {
+        a.xs_c = 1; a.xs_w = p.C; a.xs_h = (int64_t)p.W * p.C; a.xs_d = hw * p.C;
+        a.ys_c = 1; a.ys_p = p.OC;
+    } else {
+        a.xs_c = (int64_t)p.D * hw; a.xs_d = hw; a.xs_h = p.W; a.xs_w = 1;
+        a.ys_c = p.out_vol; a.ys_p = 1;
+    }
     switch (p.dtype) {
-    case GBCONV_F32: return launch_ffma_typed<float>(a, s);
-    case GBCONV_F16: return launch_ffma_typed<__half>(a, s);
-    default: return launch_ffma_typed<__nv_bfloat16>(a, s);
+    case GBCONV_F32: return launch_ffma_typed<float>(a, p.cl, s);
+    case GBCONV_F16: return launch_ffma_typed<__half>(a, p.cl, s);
+    default: return launch_ffma_typed<__nv_bfloat16>(a, p.cl, s);
     }
 }
 

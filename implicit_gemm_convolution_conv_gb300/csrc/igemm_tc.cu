@@ -20,7 +20,10 @@
 // epilogue warps (two per lane quadrant, alternate 32-pixel chunks) reads 32
 // consecutive pixels of one channel per thread with tcgen05.ld, adds the
 // bias, applies ReLU, rounds to fp16/bf16 and writes 16-byte vectors
-// straight from registers into the NCHW/NCDHW output.
+// straight from registers into the NCHW/NCDHW output. For channels-last
+// output the 32 threads of a warp hold 32 consecutive channels of one pixel:
+// neighbouring lanes swap one value so that each lane holds two channels of
+// one pixel, and a warp store writes two pixels' 64-byte channel runs.
 //
 // Every wait on an mbarrier is bounded (SM cycle counter); on expiry the
 // kernel records an error word, lets its own in-flight copies and MMAs land,
@@ -78,6 +81,8 @@ struct TcArgs {
     int stages;
     int relu;
     int vec_store;         // 16-byte stores of 8 pixels (aligned rows and tiles)
+    int cl;                // channels-last output [N][OD][OH][OW][OC]
+    int pair_store;        // channels-last: 4-byte stores of channel pairs (OC even, y 4-byte aligned)
     uint32_t idesc;
     uint32_t tx_bytes;
     uint32_t tmem_cols;
@@ -270,6 +275,50 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const int oc = tc.oc0 + q * 32 + lane;
             const bool oc_ok = oc < a.OC;
             const float bias = (a.b && oc_ok) ? __ldg(a.b + oc) : 0.0f;
+            if (a.cl) {
+                // Channels-last: pixel p of the tile is at ((n OD + od) OH +
+                // oh0 + r) OW + ow0 + c, its channel oc at that times OC + oc.
+                T *yt = static_cast<T *>(a.y) + ((int64_t)tc.n * a.OD + tc.od) * plane * a.OC;
+                const bool odd = lane & 1;
+                const int oc_even = oc - (odd ? 1 : 0);
+                for (int ch = grp; ch < nchunks; ch += 2) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.NP + ch * kColChunk), v);
+                    tmem_ld_wait();
+                    const int p0 = ch * kColChunk;
+#pragma unroll
+                    for (int e = 0; e < kColChunk; e += 2) {
+                        const float v0 = epilogue(__uint_as_float(v[e]), bias, a.relu);
+                        const float v1 = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
+                        if (a.pair_store) {
+                            // Even lanes keep pixel e, odd lanes pixel e + 1;
+                            // each lane gets its partner's value of that pixel.
+                            const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                            const int p = p0 + e + (odd ? 1 : 0);
+                            const int r = p / a.BW, c = p - r * a.BW;
+                            if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW && oc_even < a.OC) {
+                                const float lo = odd ? got : v0, hi = odd ? v1 : got;
+                                typename Storage<T>::Pair pr = Storage<T>::pack2(lo, hi);
+                                *reinterpret_cast<typename Storage<T>::Pair *>(
+                                    yt + ((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc_even) = pr;
+                            }
+                        } else if (oc_ok) {
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int p = p0 + e + u;
+                                const int r = p / a.BW, c = p - r * a.BW;
+                                if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
+                                    yt[((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc] =
+                                        Storage<T>::from_float(u ? v1 : v0);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+                continue;
+            }
             T *yc = static_cast<T *>(a.y) +
                     ((int64_t)tc.n * a.OC + (oc_ok ? oc : 0)) * a.OD * plane + (int64_t)tc.od * plane;
             for (int ch = grp; ch < nchunks; ch += 2) {
@@ -536,6 +585,8 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.stages = g.stages;
     a.relu = p.act == GBCONV_ACT_RELU;
     a.vec_store = (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
+    a.cl = p.cl;
+    a.pair_store = (p.OC % 2 == 0) && (((uintptr_t)y % 4) == 0);
     a.idesc = make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
     a.tx_bytes = kWStageBytes + 128u * (uint32_t)(g.BW * g.BH);
     {

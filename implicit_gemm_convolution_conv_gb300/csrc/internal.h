@@ -23,11 +23,14 @@ struct Problem {
     int64_t x_elems, w_elems, y_elems;
     int64_t out_vol;          // OD * OH * OW (convolution output)
     int pool;                 // 1: 2x2 stride-2 max pool fused after the activation
+    int cl;                   // 1: channels-last x [N][D][H][W][C] and y [N][OD][OH][OW][OC]
     int YH, YW;               // stored output rows / columns (OH/2, OW/2 when pooled)
     int64_t in_vol;           // D * H * W
     int elt;                  // bytes per stored element
 };
 
+// The tensor-core path can read channels-last x in place: 16-byte rows.
+inline bool tc_cl_direct(const Problem &p) { return p.cl && p.C % 8 == 0; }
 // Tensor-core path channel padding: channels-last copies and packed weights
 // carry C rounded up to a multiple of 8 (16-byte rows for TMA).
 inline int tc_cpad(int C) { return (C + 7) / 8 * 8; }

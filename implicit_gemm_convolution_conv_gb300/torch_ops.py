@@ -34,16 +34,22 @@ def to_numpy(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
-def _desc(x, OC, k, stride, pad, relu, algo, w_layout, tpad=0, pool=False):
+def _desc(x, OC, k, stride, pad, relu, algo, w_layout, tpad=0, pool=False,
+          channels_last=False):
     nsp = x.dim() - 2
-    if nsp == 2:
+    if channels_last:
+        # x is [N, H, W, C] or [N, D, H, W, C]
+        N, C = x.shape[0], x.shape[-1]
+        D, H, W = (1,) + tuple(x.shape[1:3]) if nsp == 2 else tuple(x.shape[1:4])
+    elif nsp == 2:
         N, C, H, W = x.shape
         D = 1
     else:
         N, C, D, H, W = x.shape
     d = make_desc(N, C, H, W, OC, k=k, pad=pad, stride=stride, D=D,
                   dtype=CODE_OF[x.dtype], act=ACT_RELU if relu else ACT_NONE,
-                  w_layout=w_layout, algo=algo, tpad=tpad, pool=pool)
+                  w_layout=w_layout, algo=algo, tpad=tpad, pool=pool,
+                  channels_last=channels_last)
     return d, nsp
 
 
@@ -56,16 +62,19 @@ class Conv:
     """A prepared convolution: descriptor, output and workspace allocated once.
 
     `w` is OIHW/OIDHW; with `prepack=True` it is packed once with
-    gbconv_weight_pack and later calls pass w_layout PACKED.
+    gbconv_weight_pack and later calls pass w_layout PACKED. With
+    `channels_last=True`, x is [N, (D,) H, W, C] and y [N, (OD,) OH, OW, OC].
     """
 
     def __init__(self, x, w, b=None, stride=1, pad=0, relu=False,
                  algo=ALGO_AUTO, prepack=False, out=None, workspace=None, tpad=0,
-                 pool=False):
+                 pool=False, channels_last=False):
         self.x, self.b = x, b
         OC, k = w.shape[0], w.shape[-1]
         layout = W_PACKED if prepack else W_OIHW
-        self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout, tpad, pool)
+        self.channels_last = channels_last
+        self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout, tpad, pool,
+                                    channels_last)
         st, self.algo = select_algo(self.desc, self.nsp)
         check(st)
         if prepack:
@@ -90,7 +99,8 @@ class Conv:
             st, (od, oh, ow) = output_shape(self.desc, self.nsp)
             check(st)
             sp = [oh, ow] if self.nsp == 2 else [od, oh, ow]
-            out = torch.empty([x.shape[0], OC] + sp, dtype=x.dtype, device=x.device)
+            shape = [x.shape[0]] + sp + [OC] if channels_last else [x.shape[0], OC] + sp
+            out = torch.empty(shape, dtype=x.dtype, device=x.device)
         self.y = out
         self._fn = conv2d_fwd if self.nsp == 2 else conv3d_fwd
 
@@ -116,6 +126,7 @@ def _aligned_view(raw: torch.Tensor, nbytes: int) -> torch.Tensor:
 
 
 def forward(x, w, b=None, stride=1, pad=0, relu=False, algo=ALGO_AUTO,
-            prepack=False, tpad=0, pool=False):
+            prepack=False, tpad=0, pool=False, channels_last=False):
     """One convolution call; returns y (allocated here)."""
-    return Conv(x, w, b, stride, pad, relu, algo, prepack, tpad=tpad, pool=pool)()
+    return Conv(x, w, b, stride, pad, relu, algo, prepack, tpad=tpad, pool=pool,
+                channels_last=channels_last)()

@@ -17,7 +17,8 @@
  *
  * Output extent per axis: O = floor((I + 2*pad - k) / stride) + 1.
  *
- * Layouts (all densely packed, row-major, element offsets):
+ * Layouts (all densely packed, row-major, element offsets; x and y may
+ * instead be channels-last, see GBCONV_FLAG_CHANNELS_LAST):
  *   x  conv2d [N][C][H][W]        conv3d [N][C][D][H][W]
  *   w  conv2d [OC][C][k][k]       conv3d [OC][C][k][k][k]   (w_layout OIHW)
  *      or the opaque packed form written by gbconv_weight_pack (w_layout PACKED)
@@ -129,6 +130,23 @@ typedef enum gbconv_tpad {
  * pad <= 1); other shapes or algorithms return GBCONV_ERR_ALGO.
  */
 #define GBCONV_FLAG_MAXPOOL2 0x4
+/*
+ * Bit 3 of gbconv_desc.flags: channels-last activations. x is
+ * [N][H][W][C] (conv2d) or [N][D][H][W][C] (conv3d) and y is
+ * [N][OH][OW][OC] or [N][OD][OH][OW][OC]; weights keep their layout (OIHW /
+ * OIDHW or packed). With channels-last output feeding channels-last input,
+ * convolutions chain with no re-layout between them, the way
+ * git.erdda.com/Tencent/ncnn/discussions/7001 (SeedVR2, limitations and
+ * roadmap) plans to keep its packed channel layout across the video-VAE's
+ * layers; lpnh.cn/news/2745477 section 2.3 weighs NHWC's vector-friendly
+ * channel runs against NCHW's simplicity.
+ * Kernels: the tensor-core implicit GEMM (float16/bfloat16, C a multiple of
+ * 8, x 16-byte aligned; it reads x in place, so the call needs no
+ * channels-last copy in the workspace) and the CUDA-core implicit GEMM (any
+ * dtype and C). AUTO picks the first when it applies, else the second; the
+ * direct kernels and the fused max pool return GBCONV_ERR_ALGO.
+ */
+#define GBCONV_FLAG_CHANNELS_LAST 0x8
 
 /*
  * Problem descriptor. Zero-initialise it, then set every field you use.
@@ -143,7 +161,8 @@ typedef struct gbconv_desc {
     int act;                  /* gbconv_act */
     int w_layout;             /* gbconv_wlayout */
     int algo;                 /* gbconv_algo */
-    int flags;                /* bits 0-1: gbconv_tpad (conv3d frame padding); other bits must be 0 */
+    int flags;                /* bits 0-1: gbconv_tpad (conv3d frame padding); bit 2: fused 2x2 max
+                                 pool; bit 3: channels-last x and y; other bits must be 0 */
     void *workspace;          /* device scratch, >= gbconv_workspace_size bytes, 256-B aligned */
     size_t workspace_bytes;
 } gbconv_desc;

@@ -44,6 +44,8 @@ class Layer:
     seed: int = 20260
     tpad: int = 0               # conv3d frame padding: 0 symmetric, 1 causal (k-1 front), 2 none
     pool: bool = False          # 2x2 stride-2 max pool fused after the activation (2D)
+    cl: bool = False            # channels-last x and y on the device (layout only; the
+                                # arrays drawn here stay NC(D)HW)
 
     @property
     def kvol(self) -> int:

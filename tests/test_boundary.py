@@ -82,7 +82,7 @@ BAD = [
     (dict(dtype=3), gb.ERR_DTYPE), (dict(dtype=-1), gb.ERR_DTYPE),
     (dict(act=2), gb.ERR_ACT), (dict(act=-7), gb.ERR_ACT),
     (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, C=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, OC=129), gb.ERR_ALGO),
-    (dict(flags=8), gb.ERR_RESERVED), (dict(flags=3), gb.ERR_RESERVED),
+    (dict(flags=16), gb.ERR_RESERVED), (dict(flags=3), gb.ERR_RESERVED),
     (dict(tpad=gb.TPAD_CAUSAL), gb.ERR_SHAPE),      # conv2d: symmetric frames only
     (dict(algo=gb.ALGO_IGEMM_TC), gb.ERR_ALGO),     # tensor cores need 16-bit
     (dict(C=64, algo=gb.ALGO_DIRECT, k=15, pad=7, H=64, W=64, OC=32),
@@ -193,6 +193,38 @@ def test_fused_maxpool_shapes_and_limits():
     assert gb.output_shape(mk(H=1, W=8, pad=0, k=1), 2)[0] == gb.ERR_SHAPE
     d3 = gb.make_desc(1, 3, 8, 8, 4, 3, 1, 1, D=4, pool=True)
     assert gb.output_shape(d3, 3)[0] == gb.ERR_SHAPE
+
+
+def test_channels_last_algorithms_and_workspace():
+    """Channels-last x and y: the tensor-core GEMM for 16-bit storage with C a
+    multiple of 8 (reading x in place: no channels-last copy in the
+    workspace), else the CUDA-core GEMM; the direct kernels and the fused pool
+    refuse the flag."""
+    cl = lambda **kw: _desc(**dict(dict(channels_last=True), **kw))
+    pick = lambda d, nd=2: gb.select_algo(d, nd)
+    assert pick(cl(C=64, OC=64, dtype=gb.F16)) == (gb.OK, gb.ALGO_IGEMM_TC)
+    assert pick(cl(C=64, OC=64, dtype=gb.BF16)) == (gb.OK, gb.ALGO_IGEMM_TC)
+    assert pick(cl(C=12, OC=64, dtype=gb.F16)) == (gb.OK, gb.ALGO_IGEMM_FFMA)
+    assert pick(cl(C=3, OC=32, H=640, W=640, stride=2)) == (gb.OK, gb.ALGO_IGEMM_FFMA)
+    assert pick(cl(C=64, OC=64)) == (gb.OK, gb.ALGO_IGEMM_FFMA)
+    assert pick(cl(C=3, OC=8, algo=gb.ALGO_DIRECT))[0] == gb.ERR_ALGO
+    assert pick(cl(C=3, OC=32, algo=gb.ALGO_DIRECT_TC))[0] == gb.ERR_ALGO
+    assert pick(cl(C=12, OC=64, dtype=gb.F16, algo=gb.ALGO_IGEMM_TC))[0] == gb.ERR_ALGO
+    assert pick(cl(C=3, OC=32, pool=True))[0] == gb.ERR_ALGO
+    d3 = gb.make_desc(1, 128, 128, 240, 128, 3, 1, 1, D=5, dtype=gb.F16, channels_last=True)
+    assert pick(d3, 3) == (gb.OK, gb.ALGO_IGEMM_TC)
+    assert gb.output_shape(d3, 3) == (gb.OK, (5, 128, 240))
+    # workspace: packed weights only, and nothing once they are pre-packed
+    w_pk = 27 * 128 * 128 * 2
+    assert gb.workspace_size(d3, 3) == (gb.OK, (w_pk + 255) // 256 * 256)
+    d3.w_layout = gb.W_PACKED
+    assert gb.workspace_size(d3, 3) == (gb.OK, 0)
+    # the tensor-core kernel reads x in place with TMA: 16-byte alignment
+    dh = cl(C=64, OC=64, dtype=gb.F16, w_layout=gb.W_PACKED)
+    assert gb.conv2d_fwd(dh, FAKE + 8, FAKE * 64, None, FAKE * 128, 0) == gb.ERR_ALIGN
+    # the CUDA-core path takes element alignment
+    df = cl(C=12, OC=64, dtype=gb.F16, w_layout=gb.W_PACKED)
+    assert gb.conv2d_fwd(df, FAKE + 8, FAKE * 64, None, FAKE * 128, 0) != gb.ERR_ALIGN
 
 
 def test_frame_padding_modes_shapes():
