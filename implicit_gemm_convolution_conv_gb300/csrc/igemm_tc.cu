@@ -20,10 +20,17 @@
 // epilogue warps (two per lane quadrant, alternate 32-pixel chunks) reads 32
 // consecutive pixels of one channel per thread with tcgen05.ld, adds the
 // bias, applies ReLU, rounds to fp16/bf16 and writes 16-byte vectors
-// straight from registers into the NCHW/NCDHW output. For channels-last
-// output the 32 threads of a warp hold 32 consecutive channels of one pixel:
-// neighbouring lanes swap one value so that each lane holds two channels of
-// one pixel, and a warp store writes two pixels' 64-byte channel runs.
+// into the output. A warp's 32 channels x 32 pixels go through a 2 KB
+// staging tile in shared memory (64-byte swizzle) and leave as one TMA tensor
+// store, [channel][pixel] for NCHW/NCDHW output and [pixel][channel] for
+// channels-last output; two staging tiles per warp let a store drain while the
+// next chunk is converted. (Stores from registers, 16-byte pixel vectors into
+// 32 different channel planes per warp instruction, cost the video-VAE
+// Convolution3D a tenth of its time.) Chunks that no single box can cover (a
+// chunk folded over two rows of the tile and not clipped by the image edge,
+// or an unaligned output) are stored from registers. For channels-last
+// output, neighbouring lanes swap one value so that each lane holds two
+// channels of one pixel.
 //
 // Every wait on an mbarrier is bounded (SM cycle counter); on expiry the
 // kernel records an error word, lets its own in-flight copies and MMAs land,
@@ -67,6 +74,8 @@ constexpr int kBlockK = 64;                       // channels per stage: one 128
 constexpr int kTileOc = 128;                      // MMA M: output channels per tile
 constexpr uint32_t kWStageBytes = 128u * 128u;    // 128 channel rows x 128 B
 constexpr int kColChunk = 32;                     // accumulator columns per tcgen05.ld
+constexpr uint32_t kYChunkBytes = 32u * 32u * 2u;  // one warp's staged 32 x 32 outputs
+constexpr uint32_t kYStageBytes = (uint32_t)kEpiWarps * 2u * kYChunkBytes;   // two per epilogue warp
 
 struct TcArgs {
     const float *b;
@@ -83,6 +92,7 @@ struct TcArgs {
     int vec_store;         // 16-byte stores of 8 pixels (aligned rows and tiles)
     int cl;                // channels-last output [N][OD][OH][OW][OC]
     int pair_store;        // channels-last: 4-byte stores of channel pairs (OC even, y 4-byte aligned)
+    int tma_store;         // staged chunks leave as TMA tensor stores (tmY valid)
     uint32_t idesc;
     uint32_t tx_bytes;
     uint32_t tmem_cols;
@@ -114,14 +124,15 @@ __device__ __forceinline__ TileCoord tile_coord(const TcArgs &a, int t) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const TcArgs a) {
+                const __grid_constant__ CUtensorMap tmY, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t x_stage = (uint32_t)a.NP * 128u;
     const uint32_t sW = base;
     const uint32_t sX = sW + (uint32_t)a.stages * kWStageBytes;
-    const uint32_t sBar = sX + (uint32_t)a.stages * x_stage;
+    const uint32_t sY = sX + (uint32_t)a.stages * x_stage;     // epilogue staging (1024-aligned)
+    const uint32_t sBar = sY + kYStageBytes;
     const uint32_t full0 = sBar, empty0 = sBar + 8u * kMaxStages;
     const uint32_t tfull0 = sBar + 16u * kMaxStages, tempty0 = tfull0 + 16u;
     const uint32_t drain_bar = tempty0 + 16u;
@@ -147,6 +158,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
+        if (a.tma_store) prefetch_tmap(&tmY);
     }
     if (warp == 1) {
         tmem_alloc(slot_addr, a.tmem_cols);
@@ -259,6 +271,8 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int MT = a.BW * a.BH;
         const int nchunks = (MT + kColChunk - 1) / kColChunk;
         const int64_t plane = (int64_t)a.OH * a.OW;
+        const uint32_t ystage = sY + (uint32_t)(warp - 2) * 2u * kYChunkBytes;
+        int nst = 0;             // TMA stores this warp has issued
         int local = 0;
         for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++local) {
             const TileCoord tc = tile_coord(a, t);
@@ -275,85 +289,162 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const int oc = tc.oc0 + q * 32 + lane;
             const bool oc_ok = oc < a.OC;
             const float bias = (a.b && oc_ok) ? __ldg(a.b + oc) : 0.0f;
-            if (a.cl) {
-                // Channels-last: pixel p of the tile is at ((n OD + od) OH +
-                // oh0 + r) OW + ow0 + c, its channel oc at that times OC + oc.
-                T *yt = static_cast<T *>(a.y) + ((int64_t)tc.n * a.OD + tc.od) * plane * a.OC;
-                const bool odd = lane & 1;
-                const int oc_even = oc - (odd ? 1 : 0);
-                for (int ch = grp; ch < nchunks; ch += 2) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.NP + ch * kColChunk), v);
-                    tmem_ld_wait();
-                    const int p0 = ch * kColChunk;
+            const bool odd = lane & 1;
+            const int oc_even = oc - (odd ? 1 : 0);
+            // Channels-last: pixel (r, c) of the tile is at ((n OD + od) OH +
+            // oh0 + r) OW + ow0 + c, its channel oc at that times OC + oc.
+            // NCHW: channel oc's plane, pixel at (oh0 + r) OW + ow0 + c.
+            T *const ybase = a.cl ? static_cast<T *>(a.y) + ((int64_t)tc.n * a.OD + tc.od) * plane * a.OC
+                                  : static_cast<T *>(a.y) +
+                                        ((int64_t)tc.n * a.OC + (oc_ok ? oc : 0)) * a.OD * plane +
+                                        (int64_t)tc.od * plane;
+            // One 32-pixel chunk: its first pixel is row r0, column c0 of the
+            // tile. A chunk that lies in one row and inside the output takes
+            // the unchecked path; others step (r, c) pixel by pixel.
+            auto store_chunk = [&](const uint32_t (&v)[32], int ch) {
+                const int p0 = ch * kColChunk;
+                const int r0 = p0 / a.BW, c0 = p0 - r0 * a.BW;
+                const bool whole = c0 + kColChunk <= a.BW && r0 < a.BH && tc.oh0 + r0 < a.OH &&
+                                   tc.ow0 + c0 + kColChunk <= a.OW;
+                const int64_t pix0 = (int64_t)(tc.oh0 + r0) * a.OW + tc.ow0 + c0;
+                // One box: the chunk lies in row r0 of the tile, or runs past
+                // the tile's last row only where the image edge clips it.
+                if (a.tma_store && r0 < a.BH &&
+                    (c0 + kColChunk <= a.BW || (r0 == a.BH - 1 && tc.ow0 + a.BW >= a.OW))) {
+                    if (tc.oh0 + r0 >= a.OH) return;
+                    const uint32_t buf = ystage + (uint32_t)(nst & 1) * kYChunkBytes;
+                    if (nst >= 2) {
+                        // The store that last used this buffer has read it.
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+                    }
+                    if (a.cl) {
+                        // [pixel][channel] rows of 64 B; 16-byte unit u of row e
+                        // sits at unit u ^ ((e >> 1) & 3) (64-byte swizzle).
+                        const uint32_t cb = (uint32_t)(lane & ~1) * 2u;      // byte of channel pair
 #pragma unroll
-                    for (int e = 0; e < kColChunk; e += 2) {
-                        const float v0 = epilogue(__uint_as_float(v[e]), bias, a.relu);
-                        const float v1 = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
-                        if (a.pair_store) {
-                            // Even lanes keep pixel e, odd lanes pixel e + 1;
-                            // each lane gets its partner's value of that pixel.
+                        for (int e = 0; e < kColChunk; e += 2) {
+                            const float v0 = epilogue(__uint_as_float(v[e]), bias, a.relu);
+                            const float v1 = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
                             const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-                            const int p = p0 + e + (odd ? 1 : 0);
-                            const int r = p / a.BW, c = p - r * a.BW;
-                            if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW && oc_even < a.OC) {
-                                const float lo = odd ? got : v0, hi = odd ? v1 : got;
-                                typename Storage<T>::Pair pr = Storage<T>::pack2(lo, hi);
-                                *reinterpret_cast<typename Storage<T>::Pair *>(
-                                    yt + ((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc_even) = pr;
-                            }
-                        } else if (oc_ok) {
+                            const typename Storage<T>::Pair pr = Storage<T>::pack2(odd ? got : v0, odd ? v1 : got);
+                            const int row = e + (odd ? 1 : 0);
+                            const uint32_t addr = buf + (uint32_t)row * 64u +
+                                                  ((((cb >> 4) ^ (uint32_t)((row >> 1) & 3)) << 4) | (cb & 15u));
+                            asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr),
+                                         "r"(*reinterpret_cast<const uint32_t *>(&pr))
+                                         : "memory");
+                        }
+                    } else {
+                        // [channel][pixel] rows of 64 B: this lane's channel, 32 pixels.
 #pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int p = p0 + e + u;
-                                const int r = p / a.BW, c = p - r * a.BW;
-                                if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
-                                    yt[((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc] =
-                                        Storage<T>::from_float(u ? v1 : v0);
-                            }
+                        for (int u = 0; u < 4; ++u) {
+                            typename Storage<T>::Pair h[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                h[e] = Storage<T>::pack2(epilogue(__uint_as_float(v[8 * u + 2 * e]), bias, a.relu),
+                                                         epilogue(__uint_as_float(v[8 * u + 2 * e + 1]), bias, a.relu));
+                            const uint32_t addr = buf + (uint32_t)lane * 64u +
+                                                  (((uint32_t)u ^ (uint32_t)((lane >> 1) & 3)) << 4);
+                            const uint4 hv = *reinterpret_cast<const uint4 *>(h);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(hv.x), "r"(hv.y),
+                                         "r"(hv.z), "r"(hv.w)
+                                         : "memory");
                         }
                     }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int chan = tc.oc0 + q * 32;
+                        if (a.cl)
+                            tma_store_5d(&tmY, buf, chan, tc.ow0 + c0, tc.oh0 + r0, tc.od, tc.n);
+                        else
+                            tma_store_5d(&tmY, buf, tc.ow0 + c0, tc.oh0 + r0, tc.od, chan, tc.n);
+                        bulk_commit_group();
+                    }
+                    ++nst;
+                    return;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
-                continue;
-            }
-            T *yc = static_cast<T *>(a.y) +
-                    ((int64_t)tc.n * a.OC + (oc_ok ? oc : 0)) * a.OD * plane + (int64_t)tc.od * plane;
-            for (int ch = grp; ch < nchunks; ch += 2) {
-                uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.NP + ch * kColChunk), v);
-                tmem_ld_wait();
-                if (!oc_ok) continue;
-                const int p0 = ch * kColChunk;
-                if (a.vec_store) {
+                if (a.cl) {
+                    if (a.pair_store) {
+                        // Even lanes keep pixel e, odd lanes pixel e + 1; each
+                        // lane gets its partner's value of that pixel and
+                        // stores the channel pair (oc_even, oc_even + 1).
+                        const bool oc_pair_ok = oc_even < a.OC;
+                        int r = r0, c = c0 + (odd ? 1 : 0);
+                        if (c >= a.BW) { c -= a.BW; ++r; }
+                        T *yp = ybase + (pix0 + (odd ? 1 : 0)) * a.OC + oc_even;
+#pragma unroll
+                        for (int e = 0; e < kColChunk; e += 2) {
+                            const float v0 = epilogue(__uint_as_float(v[e]), bias, a.relu);
+                            const float v1 = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
+                            const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                            const typename Storage<T>::Pair pr =
+                                Storage<T>::pack2(odd ? got : v0, odd ? v1 : got);
+                            if (whole) {
+                                if (oc_pair_ok)
+                                    *reinterpret_cast<typename Storage<T>::Pair *>(yp + (int64_t)e * a.OC) = pr;
+                            } else {
+                                if (oc_pair_ok && r < a.BH && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
+                                    *reinterpret_cast<typename Storage<T>::Pair *>(
+                                        ybase + ((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc_even) = pr;
+                                c += 2;
+                                if (c >= a.BW) { c -= a.BW; ++r; }
+                            }
+                        }
+                    } else if (oc_ok) {
+                        int r = r0, c = c0;
+#pragma unroll
+                        for (int e = 0; e < kColChunk; ++e) {
+                            if (r < a.BH && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
+                                ybase[((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc] =
+                                    Storage<T>::from_float(epilogue(__uint_as_float(v[e]), bias, a.relu));
+                            if (++c == a.BW) { c = 0; ++r; }
+                        }
+                    }
+                    return;
+                }
+                if (!oc_ok) return;
+                if (a.vec_store && whole) {
+                    // 16-byte vectors of 8 consecutive pixels (rows and tiles 8-aligned).
 #pragma unroll
                     for (int i8 = 0; i8 < kColChunk / 8; ++i8) {
-                        const int p = p0 + 8 * i8;
-                        const int r = a.BH == 1 ? 0 : p / a.BW;
-                        const int c = p - r * a.BW;
-                        if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW) {
-                            alignas(16) T h[8];
+                        typename Storage<T>::Pair h[4];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                h[e] = Storage<T>::from_float(
-                                    epilogue(__uint_as_float(v[8 * i8 + e]), bias, a.relu));
-                            *reinterpret_cast<uint4 *>(yc + (int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) =
-                                *reinterpret_cast<const uint4 *>(h);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            h[e] = Storage<T>::pack2(epilogue(__uint_as_float(v[8 * i8 + 2 * e]), bias, a.relu),
+                                                     epilogue(__uint_as_float(v[8 * i8 + 2 * e + 1]), bias, a.relu));
+                        *reinterpret_cast<uint4 *>(ybase + pix0 + 8 * i8) = *reinterpret_cast<const uint4 *>(h);
                     }
                 } else {
+                    int r = r0, c = c0;
 #pragma unroll
                     for (int e = 0; e < kColChunk; ++e) {
-                        const int p = p0 + e;
-                        const int r = p / a.BW, c = p - r * a.BW;
-                        if (p < MT && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
-                            yc[(int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c] =
+                        if (r < a.BH && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
+                            ybase[(int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c] =
                                 Storage<T>::from_float(epilogue(__uint_as_float(v[e]), bias, a.relu));
+                        if (++c == a.BW) { c = 0; ++r; }
                     }
                 }
+            };
+            // Chunks grp, grp + 2, ...: the next chunk's TMEM load is in
+            // flight while the current one is converted and stored.
+            const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.NP);
+            uint32_t va[32], vb[32];
+            int ch = grp;
+            if (ch < nchunks) tmem_ld32(tl + (uint32_t)(ch * kColChunk), va);
+            while (ch < nchunks) {
+                tmem_ld_wait();
+                if (ch + 2 < nchunks) tmem_ld32(tl + (uint32_t)((ch + 2) * kColChunk), vb);
+                store_chunk(va, ch);
+                ch += 2;
+                if (ch >= nchunks) break;
+                tmem_ld_wait();
+                if (ch + 2 < nchunks) tmem_ld32(tl + (uint32_t)((ch + 2) * kColChunk), va);
+                store_chunk(vb, ch);
+                ch += 2;
             }
+            tmem_ld_wait();
             // All reads of this accumulator by this warp are done: hand it back.
             tc_fence_before();
             __syncwarp();
@@ -361,6 +452,9 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         }
     }
 
+    // The staging tiles must have been read before the CTA's shared memory
+    // goes away; the stores' global writes complete with the grid.
+    if (warp >= 2 && lane == 0) bulk_wait_read_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -509,14 +603,14 @@ TileGeom choose_geom(const Problem &p) {
     }
     g.NP = (g.BW * g.BH + 15) / 16 * 16;
     const int stage_bytes = (int)kWStageBytes + g.NP * 128;
-    const int fixed = 1024 + 256;
+    const int fixed = 1024 + (int)kYStageBytes + 256;
     int st = (227 * 1024 - fixed) / stage_bytes;
     g.stages = st > kMaxStages ? kMaxStages : st;
     return g;
 }
 
 size_t smem_bytes(const TileGeom &g) {
-    return 1024 + (size_t)g.stages * (kWStageBytes + (size_t)g.NP * 128) + 256;
+    return 1024 + (size_t)g.stages * (kWStageBytes + (size_t)g.NP * 128) + kYStageBytes + 256;
 }
 
 uint32_t tmem_cols_for(int cols) {
@@ -538,7 +632,8 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     const CUtensorMapDataType dt =
         p.dtype == GBCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 
-    alignas(64) CUtensorMap tmX, tmW;
+    alignas(64) CUtensorMap tmX, tmW, tmY;
+    std::memset(&tmY, 0, sizeof(tmY));
     {
         // Channels-last input as {Cp, W, H, D, N}; a box is 64 channels of one
         // tile's (shifted) pixels; the conv stride is the element stride.
@@ -587,6 +682,40 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.vec_store = (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
     a.cl = p.cl;
     a.pair_store = (p.OC % 2 == 0) && (((uintptr_t)y % 4) == 0);
+    {
+        // Output as {OW, OH, OD, OC, N} (NCHW/NCDHW) or {OC, OW, OH, OD, N}
+        // (channels-last); a box is 32 pixels x 32 channels. Rows and the base
+        // 16-byte aligned, and for NCHW every box's first pixel 8-aligned.
+        const bool ok = ((uintptr_t)y % 16 == 0) &&
+                        (p.cl ? p.OC % 8 == 0 : (p.OW % 8 == 0 && g.BW % 8 == 0));
+        if (ok) {
+            const cuuint64_t e = 2;
+            cuuint64_t dims[5], strides[4];
+            cuuint32_t box[5];
+            if (p.cl) {
+                const cuuint64_t d5[5] = {(cuuint64_t)p.OC, (cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.OD,
+                                          (cuuint64_t)p.N};
+                const cuuint32_t b5[5] = {32, 32, 1, 1, 1};
+                std::memcpy(dims, d5, sizeof(d5));
+                std::memcpy(box, b5, sizeof(b5));
+            } else {
+                const cuuint64_t d5[5] = {(cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.OD, (cuuint64_t)p.OC,
+                                          (cuuint64_t)p.N};
+                const cuuint32_t b5[5] = {32, 1, 1, 32, 1};
+                std::memcpy(dims, d5, sizeof(d5));
+                std::memcpy(box, b5, sizeof(b5));
+            }
+            cuuint64_t st = e;
+            for (int i = 0; i < 4; ++i) {
+                st *= dims[i];
+                strides[i] = st;
+            }
+            const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+            a.tma_store = encode(&tmY, dt, 5, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+    }
     a.idesc = make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
     a.tx_bytes = kWStageBytes + 128u * (uint32_t)(g.BW * g.BH);
     {
@@ -608,7 +737,7 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
         attr_done.fetch_or(1ull << (dev & 63));
     }
     const int grid = num_tiles < info.sms ? (int)num_tiles : info.sms;
-    kern<<<grid, kThreads, smem, s>>>(tmX, tmW, a);
+    kern<<<grid, kThreads, smem, s>>>(tmX, tmW, tmY, a);
     return cudaGetLastError();
 }
 
