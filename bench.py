@@ -87,6 +87,13 @@ def fp32_peak_tflops(pk, sms):
     return sms * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
 
 
+def fp32_split_peak_tflops(pk):
+    """fp32 convolution FLOP rate of three TF32 products on the tensor cores:
+    the dense TF32 rate (half the bf16 rate: 1.1 vs 2.25 PFLOP/s nominal)
+    divided by the three products each fp32 product costs."""
+    return pk["bf16_tflops"] / 2 / 3
+
+
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 100 ms while running."""
@@ -314,6 +321,15 @@ def run_ours(args):
                     "frac": round(achieved / p32, 4),
                     "algorithmic_flops_per_launch": L.flops(),
                     "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+        elif L.dtype == "f32":
+            # fp32 on the tensor cores: three TF32 products per fp32 product
+            pt = fp32_split_peak_tflops(pk)
+            achieved = L.flops() / avg_s / 1e12
+            roof = {"bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": round(pt, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / pt, 4),
+                    "algorithmic_flops_per_launch": L.flops(),
+                    "peak_source": pk["source"] + " bf16_tflops / 2 (TF32 rate) / 3 (products per fp32 product)"}
         else:
             achieved = L.flops() / avg_s / 1e12
             roof = {"bound": "tensor", "achieved": round(achieved, 2),
@@ -409,6 +425,7 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
         rec = {"layer": L.name, "flop": L.flops(),
                "bytes": L.compulsory_bytes()}
         pc = p32 if L.dtype == "f32" else pk["bf16_tflops"]
+        pc_split = fp32_split_peak_tflops(pk)
         t_c = L.flops() / (pc * 1e12)
         t_m = L.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)
         t_ideal = max(t_c, t_m)
@@ -446,6 +463,11 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
                 "roofline_frac": round(t_ideal / s, 4),
                 "roofline_frac_at_3.35TBs": round(t_ideal_335 / s, 4),
                 "bound": ("tensor" if L.dtype != "f32" else "fp32") if t_c > t_m else "hbm",
+                # fp32 on the tensor cores (three TF32 products): the same
+                # time against that path's own compute ceiling
+                **({"roofline_frac_fp32_on_tensor_cores": round(
+                    max(L.flops() / (pc_split * 1e12), t_m) / s, 4)}
+                   if L.dtype == "f32" and conv.algo == gb.ALGO_IGEMM_TC else {}),
                 "compute_peak_tflops": round(pc, 1),
                 "l2": rot.l2_note,
                 "us_per_call_l2_resident": round(s_warm * 1e6, 3),

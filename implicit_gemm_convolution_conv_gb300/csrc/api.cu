@@ -86,7 +86,7 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     int algo = d->algo;
     if (algo == GBCONV_ALGO_AUTO && q.cl) {
         // Channels-last: the implicit GEMMs only (the direct kernels read NCHW).
-        algo = (q.dtype != GBCONV_F32 && tc_cl_direct(q) && tc_supported(q)) ? GBCONV_ALGO_IGEMM_TC
+        algo = ((q.dtype == GBCONV_F32 || tc_cl_direct(q)) && tc_supported(q)) ? GBCONV_ALGO_IGEMM_TC
                                                                              : GBCONV_ALGO_IGEMM_FFMA;
     } else if (algo == GBCONV_ALGO_AUTO) {
         // fp32 3x3 stems of 16+ output channels: the tensor-core stem
@@ -98,17 +98,18 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
             algo = GBCONV_ALGO_DIRECT_TC;
         else if ((int64_t)q.C * q.taps <= 64 && direct_supported(q))
             algo = GBCONV_ALGO_DIRECT;
-        else if (q.dtype != GBCONV_F32 && tc_supported(q))
-            algo = GBCONV_ALGO_IGEMM_TC;
+        else if (tc_supported(q))
+            algo = GBCONV_ALGO_IGEMM_TC;       // fp32: three TF32 products
+
         else
             algo = GBCONV_ALGO_IGEMM_FFMA;
     }
     q.algo = algo;
     if (algo == GBCONV_ALGO_DIRECT && !direct_supported(q)) return GBCONV_ERR_ALGO;
-    if (algo == GBCONV_ALGO_IGEMM_TC && (q.dtype == GBCONV_F32 || !tc_supported(q)))
-        return GBCONV_ERR_ALGO;
+    if (algo == GBCONV_ALGO_IGEMM_TC && !tc_supported(q)) return GBCONV_ERR_ALGO;
     if (algo == GBCONV_ALGO_DIRECT_TC && !stem_tc_supported(q)) return GBCONV_ERR_ALGO;
-    if (q.cl && !(algo == GBCONV_ALGO_IGEMM_FFMA || (algo == GBCONV_ALGO_IGEMM_TC && tc_cl_direct(q))))
+    if (q.cl && !(algo == GBCONV_ALGO_IGEMM_FFMA ||
+                  (algo == GBCONV_ALGO_IGEMM_TC && (tc_cl_direct(q) || q.dtype == GBCONV_F32))))
         return GBCONV_ERR_ALGO;
     // The fused pool lives in the few-channel 3x3 direct kernel only.
     if (q.pool && !(algo == GBCONV_ALGO_DIRECT && stem_supported(q))) return GBCONV_ERR_ALGO;
@@ -144,7 +145,7 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
         return GBCONV_ERR_ALIGN;
     if (p.w_layout == GBCONV_W_PACKED && !aligned(w, 256)) return GBCONV_ERR_ALIGN;
     // The tensor-core kernel reads channels-last x in place with TMA.
-    if (p.algo == GBCONV_ALGO_IGEMM_TC && p.cl && !aligned(x, 16)) return GBCONV_ERR_ALIGN;
+    if (p.algo == GBCONV_ALGO_IGEMM_TC && tc_cl_direct(p) && !aligned(x, 16)) return GBCONV_ERR_ALIGN;
     const size_t xb = (size_t)p.x_elems * p.elt, yb = (size_t)p.y_elems * p.elt;
     const size_t wb = p.w_layout == GBCONV_W_PACKED ? packed_weight_bytes(p)
                                                     : (size_t)p.w_elems * p.elt;
@@ -186,7 +187,7 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
             e = launch_pack_tc(p, w, wsp + ws.w_off, s);
             wp = wsp + ws.w_off;
         }
-        if (p.cl) {
+        if (tc_cl_direct(p)) {
             if (e == cudaSuccess) e = launch_igemm_tc(p, x, wp, b, y, s);
         } else {
             if (e == cudaSuccess) e = launch_to_channels_last(p, x, wsp + ws.x_off, s);
@@ -219,7 +220,7 @@ size_t packed_weight_bytes(const Problem &p) {
     case GBCONV_ALGO_IGEMM_FFMA:
         return (size_t)p.taps * p.C * ffma_ocpad(p.OC) * p.elt;
     case GBCONV_ALGO_IGEMM_TC:
-        return (size_t)p.taps * p.OC * tc_cpad(p.C) * p.elt;
+        return (size_t)p.taps * p.OC * tc_row_channels(p) * p.elt;
     }
     return 0;
 }
@@ -227,9 +228,10 @@ size_t packed_weight_bytes(const Problem &p) {
 Workspace workspace_layout(const Problem &p) {
     Workspace ws;
     size_t off = 0;
-    if (p.algo == GBCONV_ALGO_IGEMM_TC && !p.cl) {
+    if (p.algo == GBCONV_ALGO_IGEMM_TC && !tc_cl_direct(p)) {
+        // channels-last copy of x (16-bit) or its hi/lo split (fp32)
         ws.x_off = off;
-        ws.x_bytes = (size_t)p.N * p.in_vol * tc_cpad(p.C) * p.elt;
+        ws.x_bytes = (size_t)p.N * p.in_vol * tc_row_channels(p) * p.elt;
         off = align256(off + ws.x_bytes);
     }
     if (p.w_layout == GBCONV_W_OIHW && p.algo != GBCONV_ALGO_DIRECT && p.algo != GBCONV_ALGO_DIRECT_TC) {

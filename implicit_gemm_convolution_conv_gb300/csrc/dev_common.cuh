@@ -10,6 +10,8 @@ namespace gbconv {
 
 template <typename T> struct Storage;
 template <> struct Storage<float> {
+    using Pair = float2;
+    static __device__ __forceinline__ Pair pack2(float lo, float hi) { return make_float2(lo, hi); }
     static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
     static __device__ __forceinline__ float to_float(float v) { return v; }
     static __device__ __forceinline__ float from_float(float v) { return v; }

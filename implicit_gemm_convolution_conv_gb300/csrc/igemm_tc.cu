@@ -32,6 +32,16 @@
 // output, neighbouring lanes swap one value so that each lane holds two
 // channels of one pixel.
 //
+// fp32 storage runs on the same kernel as three TF32 products. x and the
+// packed weights carry a hi half (the value with its 13 low mantissa bits
+// cleared, exact in TF32) and a lo half (the exact remainder) along the
+// channel axis, and every 32-channel K block takes three MMA groups,
+// w_hi x_hi + w_hi x_lo + w_lo x_hi (kind::tf32), leaving about 2^-20
+// relative error per product: the split-product way to run fp32 GEMMs on
+// TF32 units. A 128-byte K block holds 32 fp32 channels as it holds 64 f16
+// ones, so the boxes, swizzle and descriptors are the same; fp32 outputs are
+// staged in 128-byte rows (128-byte swizzle).
+//
 // Every wait on an mbarrier is bounded (SM cycle counter); on expiry the
 // kernel records an error word, lets its own in-flight copies and MMAs land,
 // frees TMEM and returns.
@@ -70,12 +80,19 @@ using namespace tc;
 constexpr int kEpiWarps = 8;                      // warps 2..9, two per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxStages = 8;
-constexpr int kBlockK = 64;                       // channels per stage: one 128-B row
 constexpr int kTileOc = 128;                      // MMA M: output channels per tile
 constexpr uint32_t kWStageBytes = 128u * 128u;    // 128 channel rows x 128 B
 constexpr int kColChunk = 32;                     // accumulator columns per tcgen05.ld
-constexpr uint32_t kYChunkBytes = 32u * 32u * 2u;  // one warp's staged 32 x 32 outputs
-constexpr uint32_t kYStageBytes = (uint32_t)kEpiWarps * 2u * kYChunkBytes;   // two per epilogue warp
+// Per storage type: channels per 128-byte K block, whether fp32 is split
+// into TF32 hi/lo halves, and the epilogue's staging (a warp's 32 x 32
+// outputs, two tiles per epilogue warp).
+template <typename T>
+struct TcElt {
+    static constexpr int kBlk = 128 / (int)sizeof(T);
+    static constexpr bool kSplit = sizeof(T) == 4;
+    static constexpr uint32_t kChunkBytes = 32u * 32u * (uint32_t)sizeof(T);
+    static constexpr uint32_t kStageBytes = (uint32_t)kEpiWarps * 2u * kChunkBytes;
+};
 
 struct TcArgs {
     const float *b;
@@ -86,6 +103,8 @@ struct TcArgs {
     int tiles_w, tiles_h, oc_tiles;
     int num_tiles;
     int cblocks;
+    int cs;                // fp32 split: channels of the hi half (the lo half starts there)
+    int parts;             // MMA groups per K block: 1, or 3 for fp32 (hi.hi, hi.lo, lo.hi)
     int ksteps;
     int stages;
     int relu;
@@ -132,7 +151,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     const uint32_t sW = base;
     const uint32_t sX = sW + (uint32_t)a.stages * kWStageBytes;
     const uint32_t sY = sX + (uint32_t)a.stages * x_stage;     // epilogue staging (1024-aligned)
-    const uint32_t sBar = sY + kYStageBytes;
+    const uint32_t sBar = sY + TcElt<T>::kStageBytes;
     const uint32_t full0 = sBar, empty0 = sBar + 8u * kMaxStages;
     const uint32_t tfull0 = sBar + 16u * kMaxStages, tempty0 = tfull0 + 16u;
     const uint32_t drain_bar = tempty0 + 16u;
@@ -183,18 +202,26 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 const TileCoord tc = tile_coord(a, t);
                 const int x0 = tc.ow0 * a.stride - a.pad, y0 = tc.oh0 * a.stride - a.pad,
                           z0 = tc.od * a.stride - a.pad_d;
-                int cb = 0, tap = 0, kx = 0, ky = 0, kz = 0;
+                int cb = 0, part = 0, tap = 0, kx = 0, ky = 0, kz = 0;
                 for (int it = 0; it < a.ksteps; ++it) {
                     const uint32_t fb = full0 + 8u * s;
                     if (!wait_bounded(empty0 + 8u * s, ph ^ 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    // Channel of the weight and pixel boxes: part 1 takes the
+                    // pixels' lo half, part 2 the weights' lo half.
+                    const int c0 = cb * TcElt<T>::kBlk;
+                    const int wc = part == 2 ? a.cs + c0 : c0, xc = part == 1 ? a.cs + c0 : c0;
                     mbar_arrive_expect_tx(fb, a.tx_bytes);
-                    tma_load_3d(sW + (uint32_t)s * kWStageBytes, &tmW, fb, cb * kBlockK, tc.oc0, tap);
-                    tma_load_5d(sX + (uint32_t)s * x_stage, &tmX, fb, cb * kBlockK, x0 + kx,
-                                y0 + ky, z0 + kz, tc.n);
+                    tma_load_3d(sW + (uint32_t)s * kWStageBytes, &tmW, fb, wc, tc.oc0, tap);
+                    tma_load_5d(sX + (uint32_t)s * x_stage, &tmX, fb, xc, x0 + kx, y0 + ky, z0 + kz, tc.n);
                     ++issued;
+                    if (++part < a.parts) {
+                        if (++s == a.stages) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
+                    part = 0;
                     if (++cb == a.cblocks) {
                         cb = 0;
                         ++tap;
@@ -240,9 +267,14 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
+                    // Four MMAs of 32 bytes of K each (16 f16/bf16 or 8 tf32).
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / 16; ++kk)
-                        tc_mma(d, wd + 2u * kk, xd + 2u * kk, a.idesc, (it | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (TcElt<T>::kSplit)
+                            tc_mma_tf32(d, wd + 2u * kk, xd + 2u * kk, a.idesc, (it | kk) != 0);
+                        else
+                            tc_mma(d, wd + 2u * kk, xd + 2u * kk, a.idesc, (it | kk) != 0);
+                    }
                     tc_commit(empty0 + 8u * s);
                     wd += w_step;
                     xd += x_step;
@@ -271,7 +303,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int MT = a.BW * a.BH;
         const int nchunks = (MT + kColChunk - 1) / kColChunk;
         const int64_t plane = (int64_t)a.OH * a.OW;
-        const uint32_t ystage = sY + (uint32_t)(warp - 2) * 2u * kYChunkBytes;
+        const uint32_t ystage = sY + (uint32_t)(warp - 2) * 2u * TcElt<T>::kChunkBytes;
         int nst = 0;             // TMA stores this warp has issued
         int local = 0;
         for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++local) {
@@ -312,13 +344,41 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 if (a.tma_store && r0 < a.BH &&
                     (c0 + kColChunk <= a.BW || (r0 == a.BH - 1 && tc.ow0 + a.BW >= a.OW))) {
                     if (tc.oh0 + r0 >= a.OH) return;
-                    const uint32_t buf = ystage + (uint32_t)(nst & 1) * kYChunkBytes;
+                    const uint32_t buf = ystage + (uint32_t)(nst & 1) * TcElt<T>::kChunkBytes;
                     if (nst >= 2) {
                         // The store that last used this buffer has read it.
                         if (lane == 0) bulk_wait_read<1>();
                         __syncwarp();
                     }
-                    if (a.cl) {
+                    if constexpr (TcElt<T>::kSplit) {
+                        // fp32: rows of 128 B, 16-byte unit u of row r at unit
+                        // u ^ (r & 7) (128-byte swizzle).
+                        if (a.cl) {
+                            // [pixel][channel]: this lane's channel in every pixel row.
+#pragma unroll
+                            for (int e = 0; e < kColChunk; ++e) {
+                                const float val = epilogue(__uint_as_float(v[e]), bias, a.relu);
+                                const uint32_t addr = buf + (uint32_t)e * 128u +
+                                                      ((((uint32_t)lane >> 2) ^ (uint32_t)(e & 7)) << 4) +
+                                                      ((uint32_t)lane & 3u) * 4u;
+                                asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(val) : "memory");
+                            }
+                        } else {
+                            // [channel][pixel]: this lane's row, 32 pixels.
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                const uint32_t addr = buf + (uint32_t)lane * 128u +
+                                                      (((uint32_t)u ^ ((uint32_t)lane & 7u)) << 4);
+                                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                             "f"(epilogue(__uint_as_float(v[4 * u]), bias, a.relu)),
+                                             "f"(epilogue(__uint_as_float(v[4 * u + 1]), bias, a.relu)),
+                                             "f"(epilogue(__uint_as_float(v[4 * u + 2]), bias, a.relu)),
+                                             "f"(epilogue(__uint_as_float(v[4 * u + 3]), bias, a.relu))
+                                             : "memory");
+                            }
+                        }
+                    } else {
+                      if (a.cl) {
                         // [pixel][channel] rows of 64 B; 16-byte unit u of row e
                         // sits at unit u ^ ((e >> 1) & 3) (64-byte swizzle).
                         const uint32_t cb = (uint32_t)(lane & ~1) * 2u;      // byte of channel pair
@@ -351,6 +411,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                                          "r"(hv.z), "r"(hv.w)
                                          : "memory");
                         }
+                      }
                     }
                     fence_proxy_async_shared();
                     __syncwarp();
@@ -366,7 +427,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     return;
                 }
                 if (a.cl) {
-                    if (a.pair_store) {
+                    if (!TcElt<T>::kSplit && a.pair_store) {
                         // Even lanes keep pixel e, odd lanes pixel e + 1; each
                         // lane gets its partner's value of that pixel and
                         // stores the channel pair (oc_even, oc_even + 1).
@@ -405,7 +466,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     return;
                 }
                 if (!oc_ok) return;
-                if (a.vec_store && whole) {
+                if (!TcElt<T>::kSplit && a.vec_store && whole) {
                     // 16-byte vectors of 8 consecutive pixels (rows and tiles 8-aligned).
 #pragma unroll
                     for (int i8 = 0; i8 < kColChunk / 8; ++i8) {
@@ -584,7 +645,32 @@ struct TileGeom {
     int BW, BH, NP, stages;
 };
 
-TileGeom choose_geom(const Problem &p) {
+uint32_t ystage_bytes(const Problem &p) {
+    return p.dtype == GBCONV_F32 ? TcElt<float>::kStageBytes : TcElt<__half>::kStageBytes;
+}
+
+// Rows per tile when whole rows fit: the count whose tiles cost least on
+// `sms` SMs, a tile's MMA time taken as max(48, NP / 2) cycles per
+// instruction (the measured f16 rates: 45.5 / 48 / 64 / 128 cycles at N =
+// 32 / 64 / 128 / 256); ties go to taller tiles (fewer prologues).
+int rows_per_tile(const Problem &p, int bh_cap, int sms) {
+    int best = 1;
+    int64_t best_cost = -1;
+    const int oc_tiles = (p.OC + kTileOc - 1) / kTileOc;
+    for (int bh = bh_cap; bh >= 1; --bh) {
+        const int np = (p.OW * bh + 15) / 16 * 16;
+        const int64_t tiles = (int64_t)p.N * p.OD * ((p.OH + bh - 1) / bh) * oc_tiles;
+        const int64_t waves = (tiles + sms - 1) / sms;
+        const int64_t cost = waves * (np / 2 > 48 ? np / 2 : 48);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bh;
+        }
+    }
+    return best;
+}
+
+TileGeom choose_geom(const Problem &p, int sms) {
     TileGeom g{};
     const int bw_max = 256 / p.stride;
     if (p.OW > bw_max) {
@@ -599,18 +685,18 @@ TileGeom choose_geom(const Problem &p) {
         const int bh_max = 256 / p.stride;
         if (bh > bh_max) bh = bh_max;
         if (bh > p.OH) bh = p.OH;
-        g.BH = bh < 1 ? 1 : bh;
+        g.BH = rows_per_tile(p, bh < 1 ? 1 : bh, sms);
     }
     g.NP = (g.BW * g.BH + 15) / 16 * 16;
     const int stage_bytes = (int)kWStageBytes + g.NP * 128;
-    const int fixed = 1024 + (int)kYStageBytes + 256;
+    const int fixed = 1024 + (int)ystage_bytes(p) + 256;
     int st = (227 * 1024 - fixed) / stage_bytes;
     g.stages = st > kMaxStages ? kMaxStages : st;
     return g;
 }
 
-size_t smem_bytes(const TileGeom &g) {
-    return 1024 + (size_t)g.stages * (kWStageBytes + (size_t)g.NP * 128) + kYStageBytes + 256;
+size_t smem_bytes(const TileGeom &g, const Problem &p) {
+    return 1024 + (size_t)g.stages * (kWStageBytes + (size_t)g.NP * 128) + ystage_bytes(p) + 256;
 }
 
 uint32_t tmem_cols_for(int cols) {
@@ -627,22 +713,27 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     DevInfo info;
     cudaError_t e = dev_info(&info);
     if (e != cudaSuccess) return e;
-    const TileGeom g = choose_geom(p);
-    const int Cp = tc_cpad(p.C);
-    const CUtensorMapDataType dt =
-        p.dtype == GBCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const TileGeom g = choose_geom(p, info.sms);
+    constexpr bool split = TcElt<T>::kSplit;
+    constexpr int blk = TcElt<T>::kBlk;
+    constexpr cuuint64_t elt = sizeof(T);
+    const int Cp = tc_row_channels(p);     // channels of a staged row (both halves for fp32)
+    const CUtensorMapDataType dt = split ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                         : (p.dtype == GBCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
 
     alignas(64) CUtensorMap tmX, tmW, tmY;
     std::memset(&tmY, 0, sizeof(tmY));
     {
-        // Channels-last input as {Cp, W, H, D, N}; a box is 64 channels of one
-        // tile's (shifted) pixels; the conv stride is the element stride.
+        // Channels-last input as {Cp, W, H, D, N}; a box is one 128-byte K
+        // block of channels of one tile's (shifted) pixels; the conv stride is
+        // the element stride.
         const cuuint64_t dims[5] = {(cuuint64_t)Cp, (cuuint64_t)p.W, (cuuint64_t)p.H,
                                     (cuuint64_t)p.D, (cuuint64_t)p.N};
-        const cuuint64_t strides[4] = {(cuuint64_t)Cp * 2, (cuuint64_t)Cp * 2 * p.W,
-                                       (cuuint64_t)Cp * 2 * p.W * p.H,
-                                       (cuuint64_t)Cp * 2 * p.W * p.H * p.D};
-        const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)(g.BW * p.stride),
+        const cuuint64_t strides[4] = {(cuuint64_t)Cp * elt, (cuuint64_t)Cp * elt * p.W,
+                                       (cuuint64_t)Cp * elt * p.W * p.H,
+                                       (cuuint64_t)Cp * elt * p.W * p.H * p.D};
+        const cuuint32_t box[5] = {(cuuint32_t)blk, (cuuint32_t)(g.BW * p.stride),
                                    (cuuint32_t)(g.BH * p.stride), 1, 1};
         const cuuint32_t es[5] = {1, (cuuint32_t)p.stride, (cuuint32_t)p.stride, 1, 1};
         if (encode(&tmX, dt, 5, const_cast<void *>(xc), dims, strides, box, es,
@@ -652,10 +743,10 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
             return cudaErrorInvalidValue;
     }
     {
-        // Packed weights {Cp, OC, taps}; a box is 64 channels x 128 outputs.
+        // Packed weights {Cp, OC, taps}; a box is one K block x 128 outputs.
         const cuuint64_t dims[3] = {(cuuint64_t)Cp, (cuuint64_t)p.OC, (cuuint64_t)p.taps};
-        const cuuint64_t strides[2] = {(cuuint64_t)Cp * 2, (cuuint64_t)Cp * 2 * p.OC};
-        const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)kTileOc, 1};
+        const cuuint64_t strides[2] = {(cuuint64_t)Cp * elt, (cuuint64_t)Cp * elt * p.OC};
+        const cuuint32_t box[3] = {(cuuint32_t)blk, (cuuint32_t)kTileOc, 1};
         const cuuint32_t es[3] = {1, 1, 1};
         if (encode(&tmW, dt, 3, const_cast<void *>(wp), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -675,21 +766,24 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.oc_tiles = (p.OC + kTileOc - 1) / kTileOc;
     const int64_t num_tiles = (int64_t)p.N * p.OD * a.tiles_h * a.tiles_w * a.oc_tiles;
     a.num_tiles = (int)num_tiles;
-    a.cblocks = (Cp + kBlockK - 1) / kBlockK;
-    a.ksteps = p.taps * a.cblocks;
+    a.cs = split ? tc_split_half(p.C) : 0;
+    a.parts = split ? 3 : 1;
+    a.cblocks = split ? a.cs / blk : (Cp + blk - 1) / blk;
+    a.ksteps = p.taps * a.cblocks * a.parts;
     a.stages = g.stages;
     a.relu = p.act == GBCONV_ACT_RELU;
-    a.vec_store = (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
+    a.vec_store = !split && (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
     a.cl = p.cl;
-    a.pair_store = (p.OC % 2 == 0) && (((uintptr_t)y % 4) == 0);
+    a.pair_store = !split && (p.OC % 2 == 0) && (((uintptr_t)y % 4) == 0);
     {
         // Output as {OW, OH, OD, OC, N} (NCHW/NCDHW) or {OC, OW, OH, OD, N}
         // (channels-last); a box is 32 pixels x 32 channels. Rows and the base
-        // 16-byte aligned, and for NCHW every box's first pixel 8-aligned.
+        // 16-byte aligned, and for NCHW every box's first pixel on 16 bytes.
+        const int a16 = 16 / (int)elt;
         const bool ok = ((uintptr_t)y % 16 == 0) &&
-                        (p.cl ? p.OC % 8 == 0 : (p.OW % 8 == 0 && g.BW % 8 == 0));
+                        (p.cl ? p.OC % a16 == 0 : (p.OW % a16 == 0 && g.BW % a16 == 0));
         if (ok) {
-            const cuuint64_t e = 2;
+            const cuuint64_t e = elt;
             cuuint64_t dims[5], strides[4];
             cuuint32_t box[5];
             if (p.cl) {
@@ -712,11 +806,12 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
             }
             const cuuint32_t es[5] = {1, 1, 1, 1, 1};
             a.tma_store = encode(&tmY, dt, 5, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                 CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                 split ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_NONE,
                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
     }
-    a.idesc = make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
+    a.idesc = split ? make_idesc_tf32(kTileOc, g.NP) : make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
     a.tx_bytes = kWStageBytes + 128u * (uint32_t)(g.BW * g.BH);
     {
         // Accumulator 1's last 32-column epilogue read may run past 2 * NP.
@@ -726,7 +821,7 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     const double cyc = (double)wait_limit_ns() * (double)info.clock_khz * 1e-6;
     a.wait_limit_cycles = cyc > 9.0e18 ? (long long)9e18 : (long long)cyc;
 
-    const size_t smem = smem_bytes(g);
+    const size_t smem = smem_bytes(g, p);
     auto kern = igemm_tc_kernel<T>;
     static std::atomic<uint64_t> attr_done{0};   // one bit per device
     int dev = 0;
@@ -742,6 +837,77 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
 }
 
 #include "stem_tf32.cuh"
+
+// fp32 on the tensor cores: x -> xs [N][S][2 Cs] with xs[..][c] = hi(x) and
+// xs[..][Cs + c] = lo(x) = x - hi(x) for c < C, zero up to Cs (S = D*H*W).
+// From NC(D)HW a CTA moves 32 channels x 128 positions through a padded
+// shared tile (loads along positions, stores along channels); from
+// channels-last x each thread splits one element in place of the copy.
+constexpr int kSpC = 32, kSpS = 128;
+__global__ void __launch_bounds__(256)
+split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t S) {
+    __shared__ float tile[kSpC][kSpS + 1];
+    const int64_t s0 = (int64_t)blockIdx.x * kSpS;
+    const int c0 = blockIdx.y * kSpC;
+    const int n = blockIdx.z;
+    const float *xn = x + (int64_t)n * C * S;
+    for (int e = threadIdx.x; e < kSpC * kSpS; e += blockDim.x) {
+        const int cl = e / kSpS, sl = e % kSpS;
+        const int c = c0 + cl;
+        const int64_t sp = s0 + sl;
+        tile[cl][sl] = (c < C && sp < S) ? __ldg(xn + (int64_t)c * S + sp) : 0.0f;
+    }
+    __syncthreads();
+    float *xsn = xs + (int64_t)n * S * 2 * Cs;
+    for (int e = threadIdx.x; e < kSpC * kSpS; e += blockDim.x) {
+        const int sl = e / kSpC, cl = e % kSpC;
+        const int64_t sp = s0 + sl;
+        if (sp < S) {
+            float h, l;
+            tf32_split(tile[cl][sl], h, l);
+            xsn[sp * 2 * Cs + c0 + cl] = h;
+            xsn[sp * 2 * Cs + Cs + c0 + cl] = l;
+        }
+    }
+}
+__global__ void __launch_bounds__(256)
+split_cl_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t positions) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // position * Cs + c
+    if (i >= positions * Cs) return;
+    const int64_t sp = i / Cs;
+    const int c = (int)(i - sp * Cs);
+    float h = 0.0f, l = 0.0f;
+    if (c < C) tf32_split(__ldg(x + sp * C + c), h, l);
+    xs[sp * 2 * Cs + c] = h;
+    xs[sp * 2 * Cs + Cs + c] = l;
+}
+// w [OC][C][taps] -> wp [tap][OC][2 Cs]: the hi half, then the lo half.
+__global__ void __launch_bounds__(256)
+pack_split_kernel(const float *__restrict__ w, float *__restrict__ wp, int OC, int C, int Cs, int taps) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (tap * OC + oc) * Cs + c
+    if (i >= (int64_t)taps * OC * Cs) return;
+    const int c = (int)(i % Cs);
+    const int64_t r = i / Cs;
+    const int oc = (int)(r % OC), tap = (int)(r / OC);
+    float h = 0.0f, l = 0.0f;
+    if (c < C) tf32_split(__ldg(w + ((int64_t)oc * C + c) * taps + tap), h, l);
+    wp[r * 2 * Cs + c] = h;
+    wp[r * 2 * Cs + Cs + c] = l;
+}
+
+cudaError_t launch_split(const Problem &p, const void *x, void *xs, cudaStream_t s) {
+    const int Cs = tc_split_half(p.C);
+    const float *xf = static_cast<const float *>(x);
+    float *xo = static_cast<float *>(xs);
+    if (p.cl) {
+        const int64_t n = (int64_t)p.N * p.in_vol * Cs;
+        split_cl_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(xf, xo, p.C, Cs, (int64_t)p.N * p.in_vol);
+    } else {
+        dim3 grid((unsigned)((p.in_vol + kSpS - 1) / kSpS), (unsigned)(Cs / kSpC), (unsigned)p.N);
+        split_nchw_kernel<<<grid, 256, 0, s>>>(xf, xo, p.C, Cs, p.in_vol);
+    }
+    return cudaGetLastError();
+}
 
 template <typename T>
 cudaError_t launch_cl_typed(const Problem &p, const void *x, void *xc, cudaStream_t s) {
@@ -770,8 +936,8 @@ cudaError_t launch_pack_tc_typed(const Problem &p, const void *w, void *wp, cuda
 }  // namespace
 
 bool tc_supported(const Problem &p) {
-    if (p.dtype == GBCONV_F32) return false;
-    const TileGeom g = choose_geom(p);
+    // The SM count only shapes the row tiling, not whether the boxes fit.
+    const TileGeom g = choose_geom(p, 152);
     const int64_t mtiles = (int64_t)p.N * p.OD * ((p.OH + g.BH - 1) / g.BH) *
                            ((p.OW + g.BW - 1) / g.BW) * ((p.OC + kTileOc - 1) / kTileOc);
     return g.BW * p.stride <= 256 && g.BH * p.stride <= 256 && mtiles < 0x7FFFFFFF &&
@@ -780,6 +946,7 @@ bool tc_supported(const Problem &p) {
 
 cudaError_t launch_igemm_tc(const Problem &p, const void *xc, const void *wp, const float *b,
                             void *y, cudaStream_t s) {
+    if (p.dtype == GBCONV_F32) return launch_tc_typed<float>(p, xc, wp, b, y, s);
     if (p.dtype == GBCONV_BF16) return launch_tc_typed<__nv_bfloat16>(p, xc, wp, b, y, s);
     return launch_tc_typed<__half>(p, xc, wp, b, y, s);
 }
@@ -802,11 +969,19 @@ cudaError_t launch_stem_tc(const Problem &p, const void *x, const void *w, const
 }
 
 cudaError_t launch_to_channels_last(const Problem &p, const void *x, void *xc, cudaStream_t s) {
+    if (p.dtype == GBCONV_F32) return launch_split(p, x, xc, s);
     if (p.dtype == GBCONV_BF16) return launch_cl_typed<__nv_bfloat16>(p, x, xc, s);
     return launch_cl_typed<__half>(p, x, xc, s);
 }
 
 cudaError_t launch_pack_tc(const Problem &p, const void *w, void *wp, cudaStream_t s) {
+    if (p.dtype == GBCONV_F32) {
+        const int Cs = tc_split_half(p.C);
+        const int64_t n = (int64_t)p.taps * p.OC * Cs;
+        pack_split_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+            static_cast<const float *>(w), static_cast<float *>(wp), p.OC, p.C, Cs, p.taps);
+        return cudaGetLastError();
+    }
     if (p.dtype == GBCONV_BF16) return launch_pack_tc_typed<__nv_bfloat16>(p, w, wp, s);
     return launch_pack_tc_typed<__half>(p, w, wp, s);
 }

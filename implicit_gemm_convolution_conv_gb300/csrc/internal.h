@@ -29,11 +29,19 @@ struct Problem {
     int elt;                  // bytes per stored element
 };
 
-// The tensor-core path can read channels-last x in place: 16-byte rows.
-inline bool tc_cl_direct(const Problem &p) { return p.cl && p.C % 8 == 0; }
+// The tensor-core path can read channels-last 16-bit x in place: 16-byte rows.
+inline bool tc_cl_direct(const Problem &p) { return p.cl && p.dtype != GBCONV_F32 && p.C % 8 == 0; }
 // Tensor-core path channel padding: channels-last copies and packed weights
 // carry C rounded up to a multiple of 8 (16-byte rows for TMA).
 inline int tc_cpad(int C) { return (C + 7) / 8 * 8; }
+// fp32 on the tensor cores (three TF32 products): x and the packed weights
+// carry a hi and a lo half of Cs = C rounded up to 32 channels each (one
+// 128-byte K block per 32 channels), so a row holds 2 * Cs channels.
+inline int tc_split_half(int C) { return (C + 31) / 32 * 32; }
+// Channels of one staged row of x / of packed weights on the tensor-core path.
+inline int tc_row_channels(const Problem &p) {
+    return p.dtype == GBCONV_F32 ? 2 * tc_split_half(p.C) : tc_cpad(p.C);
+}
 // CUDA-core implicit GEMM packs OC rounded up to this multiple.
 constexpr int kFfmaOcAlign = 128;
 inline int ffma_ocpad(int OC) { return (OC + kFfmaOcAlign - 1) / kFfmaOcAlign * kFfmaOcAlign; }

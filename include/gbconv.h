@@ -95,7 +95,9 @@ typedef enum gbconv_algo {
     GBCONV_ALGO_AUTO = 0,
     GBCONV_ALGO_DIRECT = 1,      /* direct, shared-memory halo + register micro-tile (small IC*k^d) */
     GBCONV_ALGO_IGEMM_FFMA = 2,  /* implicit GEMM on CUDA cores, exact fp32 FMA */
-    GBCONV_ALGO_IGEMM_TC = 3,    /* implicit GEMM on tcgen05 tensor cores (fp16/bf16 storage) */
+    GBCONV_ALGO_IGEMM_TC = 3,    /* implicit GEMM on tcgen05 tensor cores: fp16/bf16 storage (kind::f16), or
+                                    fp32 storage as three TF32 products x_hi w_hi + x_lo w_hi + x_hi w_lo
+                                    (kind::tf32, fp32 accumulate; relative error near 2^-20 per product) */
     GBCONV_ALGO_DIRECT_TC = 4    /* fp32, 2D, k = 3, C <= 4, OC <= 128 (image stems) on tcgen05 tensor
                                     cores: x and w split into TF32 hi + lo parts, one MMA chain forms
                                     (x_hi + x_lo) * w_hi and (x_hi + x_lo) * w_lo, fp32 accumulate;
@@ -140,11 +142,12 @@ typedef enum gbconv_tpad {
  * roadmap) plans to keep its packed channel layout across the video-VAE's
  * layers; lpnh.cn/news/2745477 section 2.3 weighs NHWC's vector-friendly
  * channel runs against NCHW's simplicity.
- * Kernels: the tensor-core implicit GEMM (float16/bfloat16, C a multiple of
- * 8, x 16-byte aligned; it reads x in place, so the call needs no
- * channels-last copy in the workspace) and the CUDA-core implicit GEMM (any
- * dtype and C). AUTO picks the first when it applies, else the second; the
- * direct kernels and the fused max pool return GBCONV_ERR_ALGO.
+ * Kernels: the tensor-core implicit GEMM (float16/bfloat16 with C a multiple
+ * of 8 and x 16-byte aligned: it reads x in place, so the call needs no
+ * channels-last copy in the workspace; float32: x is split into its TF32
+ * halves in the workspace as for NCHW input) and the CUDA-core implicit GEMM
+ * (any dtype and C). AUTO picks the first when it applies, else the second;
+ * the direct kernels and the fused max pool return GBCONV_ERR_ALGO.
  */
 #define GBCONV_FLAG_CHANNELS_LAST 0x8
 
@@ -194,8 +197,8 @@ gbconv_status gbconv_output_shape(const gbconv_desc *desc, int ndim, int *OD,
 /*
  * Bytes of caller workspace the forward call needs for this desc (0 when the
  * chosen kernel needs none). Scratch holds the re-laid-out input (tensor-core
- * path: channels-last copy of x) and, with w_layout OIHW, the packed weights.
- * Host only.
+ * path: channels-last copy of x; for float32, x split into TF32 hi and lo
+ * halves) and, with w_layout OIHW, the packed weights. Host only.
  */
 gbconv_status gbconv_workspace_size(const gbconv_desc *desc, int ndim,
                                     size_t *bytes);

@@ -84,7 +84,6 @@ BAD = [
     (dict(w_layout=2), gb.ERR_LAYOUT), (dict(algo=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, C=5), gb.ERR_ALGO), (dict(algo=gb.ALGO_DIRECT_TC, OC=129), gb.ERR_ALGO),
     (dict(flags=16), gb.ERR_RESERVED), (dict(flags=3), gb.ERR_RESERVED),
     (dict(tpad=gb.TPAD_CAUSAL), gb.ERR_SHAPE),      # conv2d: symmetric frames only
-    (dict(algo=gb.ALGO_IGEMM_TC), gb.ERR_ALGO),     # tensor cores need 16-bit
     (dict(C=64, algo=gb.ALGO_DIRECT, k=15, pad=7, H=64, W=64, OC=32),
      gb.ERR_ALGO),                                  # halo does not fit smem
 ]
@@ -157,7 +156,7 @@ def test_shapes_and_algorithm_of_the_five_layers(idx):
     assert (od, oh, ow) == L.out_dims()
     st, algo = gb.select_algo(d, L.ndim)
     assert st == gb.OK
-    expect = {1: gb.ALGO_DIRECT, 2: gb.ALGO_DIRECT_TC, 3: gb.ALGO_IGEMM_FFMA,
+    expect = {1: gb.ALGO_DIRECT, 2: gb.ALGO_DIRECT_TC, 3: gb.ALGO_IGEMM_TC,
               4: gb.ALGO_IGEMM_TC, 5: gb.ALGO_IGEMM_TC}[idx]
     assert algo == expect, gb.algo_name(algo)
 
@@ -195,6 +194,27 @@ def test_fused_maxpool_shapes_and_limits():
     assert gb.output_shape(d3, 3)[0] == gb.ERR_SHAPE
 
 
+def test_fp32_tensor_core_gemm_workspace():
+    """fp32 layers beyond the direct kernels' reach run on the tensor cores as
+    three TF32 products: x and the packed weights carry a hi and a lo half of
+    C rounded up to 32 channels each; the CUDA-core GEMM stays available."""
+    L = synthetic.LAYERS[3]
+    d = gb.make_desc(L.N, L.C, L.H, L.W, L.OC, L.k, L.pad, L.stride)
+    assert gb.select_algo(d, 2) == (gb.OK, gb.ALGO_IGEMM_TC)
+    Cs = (L.C + 31) // 32 * 32
+    x_split = L.N * L.H * L.W * 2 * Cs * 4
+    w_pk = 9 * L.OC * 2 * Cs * 4
+    assert gb.weight_packed_size(d, 2) == (gb.OK, w_pk)
+    assert gb.workspace_size(d, 2) == (gb.OK, (x_split + 255) // 256 * 256 + (w_pk + 255) // 256 * 256)
+    d.algo = gb.ALGO_IGEMM_FFMA
+    assert gb.select_algo(d, 2) == (gb.OK, gb.ALGO_IGEMM_FFMA)
+    # C = 20 pads each half to 32 channels; channels-last fp32 still splits x in the workspace
+    dc = gb.make_desc(2, 20, 9, 13, 40, 3, 1, 1, channels_last=True)
+    assert gb.select_algo(dc, 2) == (gb.OK, gb.ALGO_IGEMM_TC)
+    assert gb.workspace_size(dc, 2) == (gb.OK, (2 * 9 * 13 * 64 * 4 + 255) // 256 * 256 +
+                                        (9 * 40 * 64 * 4 + 255) // 256 * 256)
+
+
 def test_channels_last_algorithms_and_workspace():
     """Channels-last x and y: the tensor-core GEMM for 16-bit storage with C a
     multiple of 8 (reading x in place: no channels-last copy in the
@@ -205,8 +225,9 @@ def test_channels_last_algorithms_and_workspace():
     assert pick(cl(C=64, OC=64, dtype=gb.F16)) == (gb.OK, gb.ALGO_IGEMM_TC)
     assert pick(cl(C=64, OC=64, dtype=gb.BF16)) == (gb.OK, gb.ALGO_IGEMM_TC)
     assert pick(cl(C=12, OC=64, dtype=gb.F16)) == (gb.OK, gb.ALGO_IGEMM_FFMA)
-    assert pick(cl(C=3, OC=32, H=640, W=640, stride=2)) == (gb.OK, gb.ALGO_IGEMM_FFMA)
-    assert pick(cl(C=64, OC=64)) == (gb.OK, gb.ALGO_IGEMM_FFMA)
+    assert pick(cl(C=3, OC=32, H=640, W=640, stride=2)) == (gb.OK, gb.ALGO_IGEMM_TC)
+    assert pick(cl(C=64, OC=64)) == (gb.OK, gb.ALGO_IGEMM_TC)
+    assert pick(cl(C=64, OC=64, algo=gb.ALGO_IGEMM_FFMA)) == (gb.OK, gb.ALGO_IGEMM_FFMA)
     assert pick(cl(C=3, OC=8, algo=gb.ALGO_DIRECT))[0] == gb.ERR_ALGO
     assert pick(cl(C=3, OC=32, algo=gb.ALGO_DIRECT_TC))[0] == gb.ERR_ALGO
     assert pick(cl(C=12, OC=64, dtype=gb.F16, algo=gb.ALGO_IGEMM_TC))[0] == gb.ERR_ALGO

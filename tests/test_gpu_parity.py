@@ -44,6 +44,17 @@ def test_layer_full_output(idx):
     assert_close(L.dtype, y, ref, L.name)
 
 
+def test_layer3_on_cuda_cores_full_output():
+    """The text-line batch through the exact-fp32 CUDA-core implicit GEMM
+    (AUTO runs it on the tensor cores as three TF32 products): every output
+    against the fp64 oracle."""
+    L = synthetic.LAYERS[3]
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp, algo=A_FFMA)
+    assert conv.algo == A_FFMA
+    assert_close(L.dtype, y, reference(inp), L.name + " on CUDA cores")
+
+
 def test_layer5_causal_frames_sampled_output():
     """The video-VAE Convolution3D shape with causal frame padding (the
     SeedVR2 decoder's conv; git.erdda.com/Tencent/ncnn/discussions/7001
@@ -151,6 +162,18 @@ SWEEP = [
     (A_TC, _L(dtype="bf16", C=64, H=9, W=72, OC=128, relu=True)),
     (A_TC, _L(dtype="bf16", C=24, D=3, H=6, W=24, OC=40, ndim=3)),
     (A_TC, _L(dtype="f16", N=3, C=200, D=2, H=5, W=240, OC=64, ndim=3)),
+    # fp32 on the tensor-core implicit GEMM (three TF32 products, x and the
+    # weights split into hi and lo halves of C rounded up to 32): several
+    # tiles, channel counts that are not multiples of 32, OC tails and two
+    # output-channel tiles, strides, k 1/3/5, 3D with causal frames, ReLU
+    (A_TC, _L(C=64, H=12, W=80, OC=128, relu=True)),
+    (A_TC, _L(N=2, C=20, H=9, W=13, OC=40)),
+    (A_TC, _L(C=48, H=17, W=61, OC=136, k=5, pad=2, bias=False)),
+    (A_TC, _L(C=16, H=12, W=14, OC=24, k=1, pad=0)),
+    (A_TC, _L(C=40, H=19, W=41, OC=32, stride=2, relu=True)),
+    (A_TC, _L(C=8, H=4, W=300, OC=16, stride=3, pad=2)),
+    (A_TC, _L(C=32, D=5, H=8, W=40, OC=32, ndim=3)),
+    (A_TC, _L(C=24, D=6, H=7, W=9, OC=20, ndim=3, stride=2, tpad=CAUSAL)),
     # fp32 stems on tensor cores (three TF32 products): C 1..3, strides 1..3,
     # ragged 32-pixel groups, OC tails within a 16-channel MMA N, N > 32
     (A_DTC, _L(C=3, H=32, W=32, OC=8)),
@@ -204,7 +227,7 @@ def test_sweep(algo, L):
 
 
 # -------------------------------------------------- packing, determinism
-@pytest.mark.parametrize("idx,algo", [(2, A_DIRECT), (3, A_FFMA), (4, A_TC)])
+@pytest.mark.parametrize("idx,algo", [(2, A_DIRECT), (3, A_FFMA), (3, A_TC), (4, A_TC)])
 def test_prepacked_weights_give_identical_output(idx, algo):
     inp = synthetic.make_inputs(synthetic.LAYERS[idx])
     y0, _ = run(inp, algo=algo)
@@ -298,6 +321,6 @@ def test_runtime_errors_on_gpu():
     y = torch.empty(L.y_shape(), dtype=x.dtype, device="cuda")
     d = gb.make_desc(L.N, L.C, L.H, L.W, L.OC, L.k, L.pad, L.stride, dtype=gb.F16)
     assert gb.conv2d_fwd(d, x, w, b, y) == gb.ERR_WORKSPACE
-    d32 = gb.make_desc(1, 3, 8, 8, 4, 3, 1, 1, algo=A_TC)
+    d32 = gb.make_desc(1, 5, 8, 8, 4, 3, 1, 1, algo=A_DTC)       # the stem kernel takes C <= 4
     assert gb.conv2d_fwd(d32, x, w, b, y) == gb.ERR_ALGO
     assert gb.conv3d_fwd(d, x, w, b, y) in (gb.ERR_WORKSPACE, gb.ERR_SHAPE)
