@@ -39,7 +39,11 @@
 // w_hi x_hi + w_hi x_lo + w_lo x_hi (kind::tf32), leaving about 2^-20
 // relative error per product: the split-product way to run fp32 GEMMs on
 // TF32 units. A 128-byte K block holds 32 fp32 channels as it holds 64 f16
-// ones, so the boxes, swizzle and descriptors are the same; fp32 outputs are
+// ones, so the swizzle and descriptors are the same. A stage holds both
+// halves of a K block, [w_hi | w_lo] (one box of a 4-D view of the packed
+// weights) and [x_hi | x_lo] (one box of a 5-D view of x for conv2d, two
+// boxes for conv3d): one thread issuing TMA gets about one box per 300
+// cycles, so the three products share each stage's loads. fp32 outputs are
 // staged in 128-byte rows (128-byte swizzle).
 //
 // Every wait on an mbarrier is bounded (SM cycle counter); on expiry the
@@ -104,7 +108,8 @@ struct TcArgs {
     int num_tiles;
     int cblocks;
     int cs;                // fp32 split: channels of the hi half (the lo half starts there)
-    int parts;             // MMA groups per K block: 1, or 3 for fp32 (hi.hi, hi.lo, lo.hi)
+    int x_paired;          // fp32 split: x_hi and x_lo come in one box (conv2d)
+    uint32_t xlo_off;      // fp32 split: byte offset of the x_lo tile in a stage (BW * BH * 128)
     int ksteps;
     int stages;
     int relu;
@@ -112,6 +117,7 @@ struct TcArgs {
     int cl;                // channels-last output [N][OD][OH][OW][OC]
     int pair_store;        // channels-last: 4-byte stores of channel pairs (OC even, y 4-byte aligned)
     int tma_store;         // staged chunks leave as TMA tensor stores (tmY valid)
+    int single_tile;       // every CTA owns at most one tile: the staging tiles reuse the stage ring
     uint32_t idesc;
     uint32_t tx_bytes;
     uint32_t tmem_cols;
@@ -147,11 +153,18 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t x_stage = (uint32_t)a.NP * 128u;
+    // A stage: weights (one 16 KB tile, or [w_hi | w_lo] for fp32), then the
+    // pixels (NP rows of 128 B, or [x_hi | x_lo] for fp32).
+    constexpr uint32_t w_stage = TcElt<T>::kSplit ? 2u * kWStageBytes : kWStageBytes;
+    const uint32_t x_stage = (TcElt<T>::kSplit ? 2u : 1u) * (uint32_t)a.NP * 128u;
     const uint32_t sW = base;
-    const uint32_t sX = sW + (uint32_t)a.stages * kWStageBytes;
-    const uint32_t sY = sX + (uint32_t)a.stages * x_stage;     // epilogue staging (1024-aligned)
-    const uint32_t sBar = sY + TcElt<T>::kStageBytes;
+    const uint32_t sX = sW + (uint32_t)a.stages * w_stage;
+    // Epilogue staging (1024-aligned): its own region, or, when every CTA
+    // owns one tile, the stage ring, which is idle once that tile's MMAs are
+    // done (all its loads were consumed; none follow).
+    const uint32_t ring_end = sX + (uint32_t)a.stages * x_stage;
+    const uint32_t sY = a.single_tile ? sW : ring_end;
+    const uint32_t sBar = a.single_tile ? ring_end : ring_end + TcElt<T>::kStageBytes;
     const uint32_t full0 = sBar, empty0 = sBar + 8u * kMaxStages;
     const uint32_t tfull0 = sBar + 16u * kMaxStages, tempty0 = tfull0 + 16u;
     const uint32_t drain_bar = tempty0 + 16u;
@@ -202,26 +215,29 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 const TileCoord tc = tile_coord(a, t);
                 const int x0 = tc.ow0 * a.stride - a.pad, y0 = tc.oh0 * a.stride - a.pad,
                           z0 = tc.od * a.stride - a.pad_d;
-                int cb = 0, part = 0, tap = 0, kx = 0, ky = 0, kz = 0;
+                int cb = 0, tap = 0, kx = 0, ky = 0, kz = 0;
                 for (int it = 0; it < a.ksteps; ++it) {
                     const uint32_t fb = full0 + 8u * s;
                     if (!wait_bounded(empty0 + 8u * s, ph ^ 1u, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    // Channel of the weight and pixel boxes: part 1 takes the
-                    // pixels' lo half, part 2 the weights' lo half.
                     const int c0 = cb * TcElt<T>::kBlk;
-                    const int wc = part == 2 ? a.cs + c0 : c0, xc = part == 1 ? a.cs + c0 : c0;
+                    const uint32_t dw = sW + (uint32_t)s * w_stage, dx = sX + (uint32_t)s * x_stage;
                     mbar_arrive_expect_tx(fb, a.tx_bytes);
-                    tma_load_3d(sW + (uint32_t)s * kWStageBytes, &tmW, fb, wc, tc.oc0, tap);
-                    tma_load_5d(sX + (uint32_t)s * x_stage, &tmX, fb, xc, x0 + kx, y0 + ky, z0 + kz, tc.n);
-                    ++issued;
-                    if (++part < a.parts) {
-                        if (++s == a.stages) { s = 0; ph ^= 1u; }
-                        continue;
+                    if constexpr (TcElt<T>::kSplit) {
+                        tma_load_4d(dw, &tmW, fb, c0, tc.oc0, 0, tap);              // [w_hi | w_lo]
+                        if (a.x_paired) {
+                            tma_load_5d(dx, &tmX, fb, c0, x0 + kx, y0 + ky, 0, tc.n);   // [x_hi | x_lo]
+                        } else {
+                            tma_load_5d(dx, &tmX, fb, c0, x0 + kx, y0 + ky, z0 + kz, tc.n);
+                            tma_load_5d(dx + a.xlo_off, &tmX, fb, a.cs + c0, x0 + kx, y0 + ky, z0 + kz, tc.n);
+                        }
+                    } else {
+                        tma_load_3d(dw, &tmW, fb, c0, tc.oc0, tap);
+                        tma_load_5d(dx, &tmX, fb, c0, x0 + kx, y0 + ky, z0 + kz, tc.n);
                     }
-                    part = 0;
+                    ++issued;
                     if (++cb == a.cblocks) {
                         cb = 0;
                         ++tap;
@@ -246,7 +262,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
             const uint64_t wdesc0 = sw128_kmajor_desc(sW), xdesc0 = sw128_kmajor_desc(sX);
-            const uint32_t w_step = kWStageBytes >> 4, x_step = x_stage >> 4;
+            const uint32_t w_step = w_stage >> 4, x_step = x_stage >> 4;
             int s = 0;
             uint32_t ph = 0;
             int local = 0;
@@ -267,12 +283,19 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
-                    // Four MMAs of 32 bytes of K each (16 f16/bf16 or 8 tf32).
+                    // Four MMAs of 32 bytes of K each (16 f16/bf16 or 8 tf32);
+                    // fp32: three groups, w_hi x_hi, w_hi x_lo, w_lo x_hi.
+                    if constexpr (TcElt<T>::kSplit) {
+                        const uint64_t wlo = wd + (kWStageBytes >> 4), xlo = xd + (a.xlo_off >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if (TcElt<T>::kSplit)
+                        for (int kk = 0; kk < 4; ++kk) {
                             tc_mma_tf32(d, wd + 2u * kk, xd + 2u * kk, a.idesc, (it | kk) != 0);
-                        else
+                            tc_mma_tf32(d, wd + 2u * kk, xlo + 2u * kk, a.idesc, 1u);
+                            tc_mma_tf32(d, wlo + 2u * kk, xd + 2u * kk, a.idesc, 1u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
                             tc_mma(d, wd + 2u * kk, xd + 2u * kk, a.idesc, (it | kk) != 0);
                     }
                     tc_commit(empty0 + 8u * s);
@@ -670,7 +693,7 @@ int rows_per_tile(const Problem &p, int bh_cap, int sms) {
     return best;
 }
 
-TileGeom choose_geom(const Problem &p, int sms) {
+TileGeom choose_geom(const Problem &p, int sms, bool *single_tile = nullptr) {
     TileGeom g{};
     const int bw_max = 256 / p.stride;
     if (p.OW > bw_max) {
@@ -688,15 +711,30 @@ TileGeom choose_geom(const Problem &p, int sms) {
         g.BH = rows_per_tile(p, bh < 1 ? 1 : bh, sms);
     }
     g.NP = (g.BW * g.BH + 15) / 16 * 16;
-    const int stage_bytes = (int)kWStageBytes + g.NP * 128;
-    const int fixed = 1024 + (int)ystage_bytes(p) + 256;
+    // One tile per CTA: the epilogue stages its outputs in the idle ring.
+    const int64_t tiles = (int64_t)p.N * p.OD * ((p.OH + g.BH - 1) / g.BH) * ((p.OW + g.BW - 1) / g.BW) *
+                          ((p.OC + kTileOc - 1) / kTileOc);
+    const bool single = tiles <= sms;
+    const int split = p.dtype == GBCONV_F32 ? 2 : 1;
+    const int stage_bytes = split * ((int)kWStageBytes + g.NP * 128);
+    const int fixed = 1024 + (single ? 0 : (int)ystage_bytes(p)) + 256;
     int st = (227 * 1024 - fixed) / stage_bytes;
     g.stages = st > kMaxStages ? kMaxStages : st;
+    if (single && (int64_t)g.stages * stage_bytes < (int64_t)ystage_bytes(p)) {
+        // (never for the tile sizes here: the ring is at least 2 x 18 KB)
+        st = (227 * 1024 - 1024 - (int)ystage_bytes(p) - 256) / stage_bytes;
+        g.stages = st > kMaxStages ? kMaxStages : st;
+        if (single_tile) *single_tile = false;
+    } else if (single_tile) {
+        *single_tile = single;
+    }
     return g;
 }
 
-size_t smem_bytes(const TileGeom &g, const Problem &p) {
-    return 1024 + (size_t)g.stages * (kWStageBytes + (size_t)g.NP * 128) + ystage_bytes(p) + 256;
+size_t smem_bytes(const TileGeom &g, const Problem &p, bool single_tile) {
+    const size_t split = p.dtype == GBCONV_F32 ? 2 : 1;
+    return 1024 + (size_t)g.stages * split * (kWStageBytes + (size_t)g.NP * 128) +
+           (single_tile ? 0 : ystage_bytes(p)) + 256;
 }
 
 uint32_t tmem_cols_for(int cols) {
@@ -713,7 +751,8 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     DevInfo info;
     cudaError_t e = dev_info(&info);
     if (e != cudaSuccess) return e;
-    const TileGeom g = choose_geom(p, info.sms);
+    bool single_tile = false;
+    const TileGeom g = choose_geom(p, info.sms, &single_tile);
     constexpr bool split = TcElt<T>::kSplit;
     constexpr int blk = TcElt<T>::kBlk;
     constexpr cuuint64_t elt = sizeof(T);
@@ -724,7 +763,22 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
 
     alignas(64) CUtensorMap tmX, tmW, tmY;
     std::memset(&tmY, 0, sizeof(tmY));
-    {
+    const int Cs = split ? tc_split_half(p.C) : 0;
+    bool x_paired = false;
+    if (split && p.D == 1 && p.pad_d == 0) {
+        // fp32 conv2d: x as {Cs, W, H, 2, N}, the half axis Cs channels apart
+        // inside a row, so one box {32, BW s, BH s, 2, 1} lands as [x_hi | x_lo].
+        const cuuint64_t dims[5] = {(cuuint64_t)Cs, (cuuint64_t)p.W, (cuuint64_t)p.H, 2, (cuuint64_t)p.N};
+        const cuuint64_t strides[4] = {(cuuint64_t)Cp * elt, (cuuint64_t)Cp * elt * p.W, (cuuint64_t)Cs * elt,
+                                       (cuuint64_t)Cp * elt * p.W * p.H};
+        const cuuint32_t box[5] = {(cuuint32_t)blk, (cuuint32_t)(g.BW * p.stride), (cuuint32_t)(g.BH * p.stride), 2,
+                                   1};
+        const cuuint32_t es[5] = {1, (cuuint32_t)p.stride, (cuuint32_t)p.stride, 1, 1};
+        x_paired = encode(&tmX, dt, 5, const_cast<void *>(xc), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    if (!x_paired) {
         // Channels-last input as {Cp, W, H, D, N}; a box is one 128-byte K
         // block of channels of one tile's (shifted) pixels; the conv stride is
         // the element stride.
@@ -742,7 +796,18 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {
+    if (split) {
+        // fp32 packed weights as {Cs, OC, 2, taps}: one box {32, 128, 2, 1}
+        // lands as [w_hi | w_lo].
+        const cuuint64_t dims[4] = {(cuuint64_t)Cs, (cuuint64_t)p.OC, 2, (cuuint64_t)p.taps};
+        const cuuint64_t strides[3] = {(cuuint64_t)Cp * elt, (cuuint64_t)Cs * elt, (cuuint64_t)Cp * elt * p.OC};
+        const cuuint32_t box[4] = {(cuuint32_t)blk, (cuuint32_t)kTileOc, 2, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (encode(&tmW, dt, 4, const_cast<void *>(wp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
         // Packed weights {Cp, OC, taps}; a box is one K block x 128 outputs.
         const cuuint64_t dims[3] = {(cuuint64_t)Cp, (cuuint64_t)p.OC, (cuuint64_t)p.taps};
         const cuuint64_t strides[2] = {(cuuint64_t)Cp * elt, (cuuint64_t)Cp * elt * p.OC};
@@ -766,10 +831,12 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.oc_tiles = (p.OC + kTileOc - 1) / kTileOc;
     const int64_t num_tiles = (int64_t)p.N * p.OD * a.tiles_h * a.tiles_w * a.oc_tiles;
     a.num_tiles = (int)num_tiles;
-    a.cs = split ? tc_split_half(p.C) : 0;
-    a.parts = split ? 3 : 1;
-    a.cblocks = split ? a.cs / blk : (Cp + blk - 1) / blk;
-    a.ksteps = p.taps * a.cblocks * a.parts;
+    a.cs = Cs;
+    a.x_paired = x_paired ? 1 : 0;
+    // x_lo: right after x_hi in a paired box; 1024-aligned when it is its own box.
+    a.xlo_off = x_paired ? 128u * (uint32_t)(g.BW * g.BH) : 128u * (uint32_t)((g.BW * g.BH + 7) / 8 * 8);
+    a.cblocks = split ? Cs / blk : (Cp + blk - 1) / blk;
+    a.ksteps = p.taps * a.cblocks;
     a.stages = g.stages;
     a.relu = p.act == GBCONV_ACT_RELU;
     a.vec_store = !split && (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
@@ -812,7 +879,7 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
         }
     }
     a.idesc = split ? make_idesc_tf32(kTileOc, g.NP) : make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
-    a.tx_bytes = kWStageBytes + 128u * (uint32_t)(g.BW * g.BH);
+    a.tx_bytes = (split ? 2u : 1u) * (kWStageBytes + 128u * (uint32_t)(g.BW * g.BH));
     {
         // Accumulator 1's last 32-column epilogue read may run past 2 * NP.
         const int last = g.NP + (g.BW * g.BH + kColChunk - 1) / kColChunk * kColChunk;
@@ -821,7 +888,8 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     const double cyc = (double)wait_limit_ns() * (double)info.clock_khz * 1e-6;
     a.wait_limit_cycles = cyc > 9.0e18 ? (long long)9e18 : (long long)cyc;
 
-    const size_t smem = smem_bytes(g, p);
+    a.single_tile = single_tile ? 1 : 0;
+    const size_t smem = smem_bytes(g, p, single_tile);
     auto kern = igemm_tc_kernel<T>;
     static std::atomic<uint64_t> attr_done{0};   // one bit per device
     int dev = 0;
