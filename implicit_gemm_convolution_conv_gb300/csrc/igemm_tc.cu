@@ -173,6 +173,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + (slot_addr + 4u - raw));
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -201,6 +202,8 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const long long limit = a.wait_limit_cycles;
+    // Set-up above overlaps the previous kernel's tail; global memory below.
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -559,6 +562,7 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(256)
 to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S) {
     __shared__ __align__(16) T tile[kClC][kClS];
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
     const int64_t s0 = (int64_t)blockIdx.x * kClS;
     const int c0 = blockIdx.y * kClC;
     const int n = blockIdx.z;
@@ -605,6 +609,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp, int taps) {
     __shared__ T tile[kPkC][kPkT + 1];
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
     const int oc = blockIdx.x;
     const int c0 = blockIdx.y * kPkC, t0 = blockIdx.z * kPkT;
     const T *src = w + (int64_t)oc * C * taps;
@@ -900,8 +905,7 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
         attr_done.fetch_or(1ull << (dev & 63));
     }
     const int grid = num_tiles < info.sms ? (int)num_tiles : info.sms;
-    kern<<<grid, kThreads, smem, s>>>(tmX, tmW, tmY, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, tmX, tmW, tmY, a);
 }
 
 #include "stem_tf32.cuh"
@@ -915,6 +919,7 @@ constexpr int kSpC = 32, kSpS = 128;
 __global__ void __launch_bounds__(256)
 split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t S) {
     __shared__ float tile[kSpC][kSpS + 1];
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
     const int64_t s0 = (int64_t)blockIdx.x * kSpS;
     const int c0 = blockIdx.y * kSpC;
     const int n = blockIdx.z;
@@ -940,6 +945,7 @@ split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, in
 }
 __global__ void __launch_bounds__(256)
 split_cl_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t positions) {
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // position * Cs + c
     if (i >= positions * Cs) return;
     const int64_t sp = i / Cs;
@@ -952,6 +958,7 @@ split_cl_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int 
 // w [OC][C][taps] -> wp [tap][OC][2 Cs]: the hi half, then the lo half.
 __global__ void __launch_bounds__(256)
 pack_split_kernel(const float *__restrict__ w, float *__restrict__ wp, int OC, int C, int Cs, int taps) {
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (tap * OC + oc) * Cs + c
     if (i >= (int64_t)taps * OC * Cs) return;
     const int c = (int)(i % Cs);
@@ -969,10 +976,11 @@ cudaError_t launch_split(const Problem &p, const void *x, void *xs, cudaStream_t
     float *xo = static_cast<float *>(xs);
     if (p.cl) {
         const int64_t n = (int64_t)p.N * p.in_vol * Cs;
-        split_cl_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(xf, xo, p.C, Cs, (int64_t)p.N * p.in_vol);
+        return launch_pdl(split_cl_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, xf, xo, p.C, Cs,
+                          (int64_t)p.N * p.in_vol);
     } else {
         dim3 grid((unsigned)((p.in_vol + kSpS - 1) / kSpS), (unsigned)(Cs / kSpC), (unsigned)p.N);
-        split_nchw_kernel<<<grid, 256, 0, s>>>(xf, xo, p.C, Cs, p.in_vol);
+        return launch_pdl(split_nchw_kernel, grid, dim3(256), 0, s, xf, xo, p.C, Cs, p.in_vol);
     }
     return cudaGetLastError();
 }
@@ -984,11 +992,11 @@ cudaError_t launch_cl_typed(const Problem &p, const void *x, void *xc, cudaStrea
     dim3 grid((unsigned)((S + kClS - 1) / kClS), (unsigned)((Cp + kClC - 1) / kClC), (unsigned)p.N);
     const bool vec = (S % 8 == 0) && ((uintptr_t)x % 16 == 0);
     if (vec)
-        to_channels_last_kernel<T, true><<<grid, 256, 0, s>>>(static_cast<const T *>(x),
-                                                              static_cast<T *>(xc), p.C, Cp, S);
+        return launch_pdl(to_channels_last_kernel<T, true>, grid, dim3(256), 0, s, static_cast<const T *>(x),
+                          static_cast<T *>(xc), p.C, Cp, S);
     else
-        to_channels_last_kernel<T, false><<<grid, 256, 0, s>>>(static_cast<const T *>(x),
-                                                               static_cast<T *>(xc), p.C, Cp, S);
+        return launch_pdl(to_channels_last_kernel<T, false>, grid, dim3(256), 0, s, static_cast<const T *>(x),
+                          static_cast<T *>(xc), p.C, Cp, S);
     return cudaGetLastError();
 }
 
@@ -996,8 +1004,8 @@ template <typename T>
 cudaError_t launch_pack_tc_typed(const Problem &p, const void *w, void *wp, cudaStream_t s) {
     const int Cp = tc_cpad(p.C);
     dim3 grid((unsigned)p.OC, (unsigned)((Cp + kPkC - 1) / kPkC), (unsigned)((p.taps + kPkT - 1) / kPkT));
-    pack_tc_kernel<T><<<grid, 256, 0, s>>>(static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.C,
-                                           Cp, p.taps);
+    return launch_pdl(pack_tc_kernel<T>, grid, dim3(256), 0, s, static_cast<const T *>(w), static_cast<T *>(wp),
+                      p.OC, p.C, Cp, p.taps);
     return cudaGetLastError();
 }
 
@@ -1046,8 +1054,8 @@ cudaError_t launch_pack_tc(const Problem &p, const void *w, void *wp, cudaStream
     if (p.dtype == GBCONV_F32) {
         const int Cs = tc_split_half(p.C);
         const int64_t n = (int64_t)p.taps * p.OC * Cs;
-        pack_split_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
-            static_cast<const float *>(w), static_cast<float *>(wp), p.OC, p.C, Cs, p.taps);
+        return launch_pdl(pack_split_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
+                          static_cast<const float *>(w), static_cast<float *>(wp), p.OC, p.C, Cs, p.taps);
         return cudaGetLastError();
     }
     if (p.dtype == GBCONV_BF16) return launch_pack_tc_typed<__nv_bfloat16>(p, w, wp, s);
