@@ -368,35 +368,57 @@ def run_ours(args):
 
     if rank == 0:
         # end to end: pinned host buffers, H2D of x, w, b and D2H of y inside
-        # the timed region, through the same C-ABI call
+        # the timed region, through the same C-ABI call. Consecutive steps
+        # rotate over three streams, each with its own device buffers (x, w,
+        # b, y, workspace), so one step's D2H overlaps the next steps' H2D
+        # and calls (more streams measured no faster); every step still
+        # copies all its inputs in and its output out.
         hx = torch.from_numpy(np.ascontiguousarray(device_x(L, inp))).pin_memory()
         hw = torch.from_numpy(np.ascontiguousarray(inp.w)).pin_memory()
         hb = torch.from_numpy(inp.b).pin_memory()
-        hy = torch.empty(conv.y.shape, dtype=conv.y.dtype).pin_memory()
         reps = min(args.steps, 200)
+        n_pipe = 3
+        pipes = []
+        for _ in range(n_pipe):
+            xj, wj, bj = torch.empty_like(x), torch.empty_like(w), torch.empty_like(b)
+            xj.copy_(x)
+            wj.copy_(w)
+            bj.copy_(b)
+            cj = Conv(xj, wj, bj, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool, channels_last=L.cl)
+            hyj = torch.empty(cj.y.shape, dtype=cj.y.dtype).pin_memory()
+            pipes.append((torch.cuda.Stream(), xj, wj, bj, cj, hyj))
+        torch.cuda.synchronize()
 
-        def e2e_step():
-            x.copy_(hx, non_blocking=True)
-            w.copy_(hw, non_blocking=True)
-            b.copy_(hb, non_blocking=True)
-            conv()
-            hy.copy_(conv.y, non_blocking=True)
-        for _ in range(3):
-            e2e_step()
+        def e2e_step(i):
+            sj, xj, wj, bj, cj, hyj = pipes[i % n_pipe]
+            with torch.cuda.stream(sj):
+                xj.copy_(hx, non_blocking=True)
+                wj.copy_(hw, non_blocking=True)
+                bj.copy_(hb, non_blocking=True)
+                cj()
+                hyj.copy_(cj.y, non_blocking=True)
+        for i in range(3 * n_pipe):
+            e2e_step(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(reps):
-            e2e_step()
+        for pj in pipes:
+            pj[0].wait_stream(stream)
+        for i in range(reps):
+            e2e_step(i)
+        for pj in pipes:
+            stream.wait_stream(pj[0])
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / reps
+        hy = pipes[0][5]
         line["e2e"] = {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 4),
                        "unit": "TFLOP/s",
                        "h2d_bytes_per_step": hx.numel() * hx.element_size() +
                        hw.numel() * hw.element_size() + hb.numel() * 4,
                        "d2h_bytes_per_step": hy.numel() * hy.element_size(),
-                       "ms_per_step": round(e2e_ms, 5)}
+                       "ms_per_step": round(e2e_ms, 5),
+                       "streams": n_pipe}
         if not args.skip_layers:
             line["per_layer"] = per_layer(gb, Conv, to_device, torch, dev,
                                           timed_calls, pk, sms)
