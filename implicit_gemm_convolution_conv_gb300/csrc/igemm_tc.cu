@@ -714,6 +714,12 @@ TileGeom choose_geom(const Problem &p, int sms, bool *single_tile = nullptr) {
         if (bh > bh_max) bh = bh_max;
         if (bh > p.OH) bh = p.OH;
         g.BH = rows_per_tile(p, bh < 1 ? 1 : bh, sms);
+        // fp32 stages hold two halves: keep the tile short enough for two of
+        // them next to the epilogue's staging.
+        while (p.dtype == GBCONV_F32 && g.BH > 1 &&
+               (227 * 1024 - 1024 - (int)ystage_bytes(p) - 256) /
+                       (2 * ((int)kWStageBytes + (g.BW * g.BH + 15) / 16 * 16 * 128)) < 2)
+            --g.BH;
     }
     g.NP = (g.BW * g.BH + 15) / 16 * 16;
     // One tile per CTA: the epilogue stages its outputs in the idle ring.

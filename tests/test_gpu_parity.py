@@ -174,6 +174,11 @@ SWEEP = [
     (A_TC, _L(C=8, H=4, W=300, OC=16, stride=3, pad=2)),
     (A_TC, _L(C=32, D=5, H=8, W=40, OC=32, ndim=3)),
     (A_TC, _L(C=24, D=6, H=7, W=9, OC=20, ndim=3, stride=2, tpad=CAUSAL)),
+    # more tiles than SMs (persistent CTAs, staging apart from the ring):
+    # fp32 and f16
+    (A_TC, _L(N=16, C=32, H=40, W=64, OC=32, relu=True)),
+    (A_TC, _L(dtype="f16", N=16, C=64, H=40, W=64, OC=64)),
+    (A_TC, _L(N=4, C=32, H=64, W=100, OC=32, bias=False)),
     # fp32 stems on tensor cores (three TF32 products): C 1..3, strides 1..3,
     # ragged 32-pixel groups, OC tails within a 16-channel MMA N, N > 32
     (A_DTC, _L(C=3, H=32, W=32, OC=8)),
