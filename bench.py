@@ -94,6 +94,25 @@ def fp32_split_peak_tflops(pk):
     return pk["bf16_tflops"] / 2 / 3
 
 
+# ------------------------------------------------------------- replicas
+def max_over_ranks(ms, world, device="cpu"):
+    """The slowest rank's time (ms) for the timed region: every rank runs
+    its own replica of the layer, so the job takes as long as the slowest."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_step, steps, world, total_ms):
+    """Whole-job throughput: the FLOP of all ranks' steps over the slowest
+    rank's time."""
+    return flop_per_step * steps * world / (total_ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 100 ms while running."""
@@ -287,13 +306,9 @@ def run_ours(args):
         e1.record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
-    total_ms = e0.elapsed_time(e1)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     flops = L.flops()
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = job_tflops(flops, args.steps, world, total_ms)
     avg_s = total_ms / args.steps * 1e-3
     iso = timed_calls(conv, 50, 3)
     line = None
