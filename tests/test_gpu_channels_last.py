@@ -77,6 +77,7 @@ SWEEP = [
     (A_TC, _L(C=32, D=3, H=8, W=24, OC=32, ndim=3)),
     (A_TC, _L(dtype="bf16", C=24, D=5, H=7, W=9, OC=16, ndim=3,
               tpad=gb.TPAD_CAUSAL, relu=True)),
+    (A_TC, _L(N=2, C=16, H=100, W=160, OC=32)),                    # a partial last wave
     # fp32 on the tensor cores: x split into TF32 halves from channels-last input
     (A_TC, _L(dtype="f32", C=20, H=11, W=13, OC=40, relu=True)),
     (A_TC, _L(dtype="f32", C=64, D=3, H=6, W=20, OC=32, ndim=3)),

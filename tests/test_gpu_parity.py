@@ -179,6 +179,9 @@ SWEEP = [
     (A_TC, _L(N=16, C=32, H=40, W=64, OC=32, relu=True)),
     (A_TC, _L(dtype="f16", N=16, C=64, H=40, W=64, OC=64)),
     (A_TC, _L(N=4, C=32, H=64, W=100, OC=32, bias=False)),
+    # more row tiles than CTAs with a partial last wave, 2D and 3D
+    (A_TC, _L(dtype="f16", N=2, C=16, H=100, W=160, OC=32, relu=True)),
+    (A_TC, _L(dtype="bf16", C=16, D=3, H=70, W=240, OC=16, ndim=3, tpad=CAUSAL)),
     # fp32 stems on tensor cores (three TF32 products): C 1..3, strides 1..3,
     # ragged 32-pixel groups, OC tails within a 16-channel MMA N, N > 32
     (A_DTC, _L(C=3, H=32, W=32, OC=8)),
