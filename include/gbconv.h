@@ -285,7 +285,8 @@ gbconv_status gbconv_set_wait_limit_ns(uint64_t ns);
  *             w_layout must be OIHW, workspace fields are ignored.
  *   x, w, b, y  caller-owned device pointers, as for gbconv_conv2d_fwd.
  * Errors: the usual validation codes; GBCONV_ERR_TOO_LARGE when the packed
- * weights (taps * C * roundup(OC, 64) elements) exceed the fixed array.
+ * weights (taps * C * roundup(OC, 128) elements of the storage type) exceed
+ * the fixed array.
  * All calls on a device share the array: calls whose kernels overlap on the
  * GPU race, so serialise them on one stream. The array keeps the last call's
  * contents; every call rewrites all of it that it reads. The first call on a
