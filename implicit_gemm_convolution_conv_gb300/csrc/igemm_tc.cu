@@ -922,6 +922,7 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
 // shared tile (loads along positions, stores along channels); from
 // channels-last x each thread splits one element in place of the copy.
 constexpr int kSpC = 32, kSpS = 128;
+template <bool VEC>
 __global__ void __launch_bounds__(256)
 split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t S) {
     __shared__ float tile[kSpC][kSpS + 1];
@@ -930,22 +931,43 @@ split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, in
     const int c0 = blockIdx.y * kSpC;
     const int n = blockIdx.z;
     const float *xn = x + (int64_t)n * C * S;
-    for (int e = threadIdx.x; e < kSpC * kSpS; e += blockDim.x) {
-        const int cl = e / kSpS, sl = e % kSpS;
+    // Loads: 4 consecutive positions of one channel per thread (16-byte
+    // vectors when S is a multiple of 4 and x 16-byte aligned).
+    for (int e = threadIdx.x; e < kSpC * kSpS / 4; e += blockDim.x) {
+        const int cl = e / (kSpS / 4), sl = (e % (kSpS / 4)) * 4;
         const int c = c0 + cl;
         const int64_t sp = s0 + sl;
-        tile[cl][sl] = (c < C && sp < S) ? __ldg(xn + (int64_t)c * S + sp) : 0.0f;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < C) {
+            if (VEC && sp + 4 <= S) {
+                v = __ldg(reinterpret_cast<const float4 *>(xn + (int64_t)c * S + sp));
+            } else {
+                if (sp < S) v.x = __ldg(xn + (int64_t)c * S + sp);
+                if (sp + 1 < S) v.y = __ldg(xn + (int64_t)c * S + sp + 1);
+                if (sp + 2 < S) v.z = __ldg(xn + (int64_t)c * S + sp + 2);
+                if (sp + 3 < S) v.w = __ldg(xn + (int64_t)c * S + sp + 3);
+            }
+        }
+        tile[cl][sl] = v.x;
+        tile[cl][sl + 1] = v.y;
+        tile[cl][sl + 2] = v.z;
+        tile[cl][sl + 3] = v.w;
     }
     __syncthreads();
+    // Stores: 4 consecutive channels of one position per thread, hi and lo
+    // halves as two 16-byte vectors (Cs is a multiple of 32).
     float *xsn = xs + (int64_t)n * S * 2 * Cs;
-    for (int e = threadIdx.x; e < kSpC * kSpS; e += blockDim.x) {
-        const int sl = e / kSpC, cl = e % kSpC;
+    for (int e = threadIdx.x; e < kSpC * kSpS / 4; e += blockDim.x) {
+        const int sl = e / (kSpC / 4), cl = (e % (kSpC / 4)) * 4;
         const int64_t sp = s0 + sl;
         if (sp < S) {
-            float h, l;
-            tf32_split(tile[cl][sl], h, l);
-            xsn[sp * 2 * Cs + c0 + cl] = h;
-            xsn[sp * 2 * Cs + Cs + c0 + cl] = l;
+            float4 h, l;
+            tf32_split(tile[cl][sl], h.x, l.x);
+            tf32_split(tile[cl + 1][sl], h.y, l.y);
+            tf32_split(tile[cl + 2][sl], h.z, l.z);
+            tf32_split(tile[cl + 3][sl], h.w, l.w);
+            *reinterpret_cast<float4 *>(xsn + sp * 2 * Cs + c0 + cl) = h;
+            *reinterpret_cast<float4 *>(xsn + sp * 2 * Cs + Cs + c0 + cl) = l;
         }
     }
 }
@@ -986,7 +1008,9 @@ cudaError_t launch_split(const Problem &p, const void *x, void *xs, cudaStream_t
                           (int64_t)p.N * p.in_vol);
     } else {
         dim3 grid((unsigned)((p.in_vol + kSpS - 1) / kSpS), (unsigned)(Cs / kSpC), (unsigned)p.N);
-        return launch_pdl(split_nchw_kernel, grid, dim3(256), 0, s, xf, xo, p.C, Cs, p.in_vol);
+        if (p.in_vol % 4 == 0 && (uintptr_t)xf % 16 == 0)
+            return launch_pdl(split_nchw_kernel<true>, grid, dim3(256), 0, s, xf, xo, p.C, Cs, p.in_vol);
+        return launch_pdl(split_nchw_kernel<false>, grid, dim3(256), 0, s, xf, xo, p.C, Cs, p.in_vol);
     }
     return cudaGetLastError();
 }
