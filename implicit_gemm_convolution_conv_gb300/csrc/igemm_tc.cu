@@ -601,9 +601,11 @@ to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int 
 }
 
 // wp[tap][oc][cp] = w[oc][c][tap] for c < C, zero for C <= cp < Cp. A CTA
-// handles one output channel, 64 channels and up to 32 taps: it reads
-// w[oc][c][tap0 ..] runs (contiguous along taps) into shared memory and
-// writes each tap's 64 channels as one 128-byte run of wp.
+// handles one output channel, 64 channels and up to 32 taps: the taps of its
+// channels are tn-element runs of w (one contiguous run of 64 * tn elements
+// when all taps fit), read with consecutive threads on consecutive elements
+// into shared memory; each tap's 64 channels then leave as one 128-byte run
+// of wp.
 constexpr int kPkC = 64, kPkT = 32;
 template <typename T>
 __global__ void __launch_bounds__(256)
@@ -612,17 +614,18 @@ pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int C
     pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
     const int oc = blockIdx.x;
     const int c0 = blockIdx.y * kPkC, t0 = blockIdx.z * kPkT;
-    const T *src = w + (int64_t)oc * C * taps;
-    for (int e = threadIdx.x; e < kPkC * kPkT; e += blockDim.x) {
-        const int cl = e / kPkT, tl = e % kPkT;
-        const int c = c0 + cl, t = t0 + tl;
-        tile[cl][tl] = (c < C && t < taps) ? src[(int64_t)c * taps + t] : T(0.0f);
+    const int tn = taps - t0 < kPkT ? taps - t0 : kPkT;
+    const T *src = w + (int64_t)oc * C * taps + t0;
+    for (int e = threadIdx.x; e < kPkC * tn; e += blockDim.x) {
+        const int cl = e / tn, tl = e - cl * tn;
+        const int c = c0 + cl;
+        tile[cl][tl] = c < C ? src[(int64_t)c * taps + tl] : T(0.0f);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < kPkC * kPkT; e += blockDim.x) {
+    for (int e = threadIdx.x; e < kPkC * tn; e += blockDim.x) {
         const int tl = e / kPkC, cl = e % kPkC;
-        const int cp = c0 + cl, t = t0 + tl;
-        if (cp < Cp && t < taps) wp[((int64_t)t * OC + oc) * Cp + cp] = tile[cl][tl];
+        const int cp = c0 + cl;
+        if (cp < Cp) wp[((int64_t)(t0 + tl) * OC + oc) * Cp + cp] = tile[cl][tl];
     }
 }
 
