@@ -182,15 +182,15 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
         break;
     }
     case GBCONV_ALGO_IGEMM_TC: {
-        const void *wp = w;
-        if (p.w_layout == GBCONV_W_OIHW) {
-            e = launch_pack_tc(p, w, wsp + ws.w_off, s);
-            wp = wsp + ws.w_off;
-        }
+        const bool oihw = p.w_layout == GBCONV_W_OIHW;
+        const void *wp = oihw ? static_cast<const void *>(wsp + ws.w_off) : w;
         if (tc_cl_direct(p)) {
+            if (oihw) e = launch_pack_tc(p, w, wsp + ws.w_off, s);
             if (e == cudaSuccess) e = launch_igemm_tc(p, x, wp, b, y, s);
         } else {
-            if (e == cudaSuccess) e = launch_to_channels_last(p, x, wsp + ws.x_off, s);
+            // the weight pack and the x layout pass share one launch
+            e = oihw ? launch_prep_tc(p, w, wsp + ws.w_off, x, wsp + ws.x_off, s)
+                     : launch_to_channels_last(p, x, wsp + ws.x_off, s);
             if (e == cudaSuccess) e = launch_igemm_tc(p, wsp + ws.x_off, wp, b, y, s);
         }
         break;

@@ -559,13 +559,11 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 // the column reads of the store phase hit 16 different banks per warp.
 constexpr int kClC = 64, kClS = 128;
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(256)
-to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S) {
-    __shared__ __align__(16) T tile[kClC][kClS];
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
-    const int64_t s0 = (int64_t)blockIdx.x * kClS;
-    const int c0 = blockIdx.y * kClC;
-    const int n = blockIdx.z;
+__device__ __forceinline__ void to_channels_last_block(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp,
+                                                       int64_t S, int bx, int by, int bz, T (*tile)[kClS]) {
+    const int64_t s0 = (int64_t)bx * kClS;
+    const int c0 = by * kClC;
+    const int n = bz;
     const T *xn = x + (int64_t)n * C * S;
     T *xcn = xc + (int64_t)n * S * Cp;
 #pragma unroll
@@ -599,6 +597,13 @@ to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int 
         }
     }
 }
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256)
+to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S) {
+    __shared__ __align__(16) T tile[kClC][kClS];
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    to_channels_last_block<T, VEC>(x, xc, C, Cp, S, blockIdx.x, blockIdx.y, blockIdx.z, tile);
+}
 
 // wp[tap][oc][cp] = w[oc][c][tap] for c < C, zero for C <= cp < Cp. A CTA
 // handles one output channel, 64 channels and up to 32 taps: the taps of its
@@ -608,12 +613,9 @@ to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int 
 // of wp.
 constexpr int kPkC = 64, kPkT = 32;
 template <typename T>
-__global__ void __launch_bounds__(256)
-pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp, int taps) {
-    __shared__ T tile[kPkC][kPkT + 1];
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
-    const int oc = blockIdx.x;
-    const int c0 = blockIdx.y * kPkC, t0 = blockIdx.z * kPkT;
+__device__ __forceinline__ void pack_tc_block(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp,
+                                              int taps, int oc, int by, int bz, T (*tile)[kPkT + 1]) {
+    const int c0 = by * kPkC, t0 = bz * kPkT;
     const int tn = taps - t0 < kPkT ? taps - t0 : kPkT;
     const T *src = w + (int64_t)oc * C * taps + t0;
     for (int e = threadIdx.x; e < kPkC * tn; e += blockDim.x) {
@@ -627,6 +629,46 @@ pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int C
         const int cp = c0 + cl;
         if (cp < Cp) wp[((int64_t)(t0 + tl) * OC + oc) * Cp + cp] = tile[cl][tl];
     }
+}
+template <typename T>
+__global__ void __launch_bounds__(256)
+pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp, int taps) {
+    __shared__ T tile[kPkC][kPkT + 1];
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    pack_tc_block<T>(w, wp, OC, C, Cp, taps, blockIdx.x, blockIdx.y, blockIdx.z, tile);
+}
+
+// CTA b of a grid that holds npk CTAs of one pass and nlay of another, the
+// pass with fewer CTAs first (measured: the other order leaves the smaller
+// pass trailing the larger one). Sets *pack and returns the index within the
+// pass.
+__device__ __forceinline__ int prep_block_index(int b, int npk, int nlay, bool *pack) {
+    if (npk <= nlay) {
+        *pack = b < npk;
+        return *pack ? b : b - npk;
+    }
+    *pack = b >= nlay;
+    return *pack ? b - nlay : b;
+}
+
+// Both passes in front of the GEMM when the weights come as OIHW: npk CTAs
+// do the weight-pack blocks (grid OC x pky x pkz, x fastest) and nlay the
+// layout blocks (grid clx x cly x N). The passes touch disjoint memory, so
+// one grid runs them side by side and the GEMM waits on one launch.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256)
+prep_tc_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S, int clx, int cly,
+               const T *__restrict__ w, T *__restrict__ wp, int OC, int taps, int pky, int npk, int nlay) {
+    __shared__ __align__(16) T tile[kClC][kClS];
+    static_assert(sizeof(T) * kPkC * (kPkT + 1) <= sizeof(T) * kClC * kClS, "pack tile fits the layout tile");
+    pdl_wait();   // dependents start when this grid completes
+    bool pack;
+    const int q = prep_block_index(blockIdx.x, npk, nlay, &pack);
+    if (pack)
+        pack_tc_block<T>(w, wp, OC, C, Cp, taps, q % OC, (q / OC) % pky, q / (OC * pky),
+                         reinterpret_cast<T (*)[kPkT + 1]>(&tile[0][0]));
+    else
+        to_channels_last_block<T, VEC>(x, xc, C, Cp, S, q % clx, (q / clx) % cly, q / (clx * cly), tile);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -926,13 +968,11 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
 // channels-last x each thread splits one element in place of the copy.
 constexpr int kSpC = 32, kSpS = 128;
 template <bool VEC>
-__global__ void __launch_bounds__(256)
-split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t S) {
-    __shared__ float tile[kSpC][kSpS + 1];
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
-    const int64_t s0 = (int64_t)blockIdx.x * kSpS;
-    const int c0 = blockIdx.y * kSpC;
-    const int n = blockIdx.z;
+__device__ __forceinline__ void split_nchw_block(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs,
+                                                 int64_t S, int bx, int by, int bz, float (*tile)[kSpS + 1]) {
+    const int64_t s0 = (int64_t)bx * kSpS;
+    const int c0 = by * kSpC;
+    const int n = bz;
     const float *xn = x + (int64_t)n * C * S;
     // Loads: 4 consecutive positions of one channel per thread (16-byte
     // vectors when S is a multiple of 4 and x 16-byte aligned).
@@ -974,10 +1014,9 @@ split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, in
         }
     }
 }
-__global__ void __launch_bounds__(256)
-split_cl_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t positions) {
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // position * Cs + c
+// Element i = position * Cs + c of the split of channels-last x.
+__device__ __forceinline__ void split_cl_elem(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs,
+                                              int64_t positions, int64_t i) {
     if (i >= positions * Cs) return;
     const int64_t sp = i / Cs;
     const int c = (int)(i - sp * Cs);
@@ -986,11 +1025,10 @@ split_cl_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int 
     xs[sp * 2 * Cs + c] = h;
     xs[sp * 2 * Cs + Cs + c] = l;
 }
-// w [OC][C][taps] -> wp [tap][OC][2 Cs]: the hi half, then the lo half.
-__global__ void __launch_bounds__(256)
-pack_split_kernel(const float *__restrict__ w, float *__restrict__ wp, int OC, int C, int Cs, int taps) {
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (tap * OC + oc) * Cs + c
+// Element i = (tap * OC + oc) * Cs + c of w [OC][C][taps] -> wp [tap][OC][2 Cs]:
+// the hi half, then the lo half.
+__device__ __forceinline__ void pack_split_elem(const float *__restrict__ w, float *__restrict__ wp, int OC, int C,
+                                                int Cs, int taps, int64_t i) {
     if (i >= (int64_t)taps * OC * Cs) return;
     const int c = (int)(i % Cs);
     const int64_t r = i / Cs;
@@ -999,6 +1037,45 @@ pack_split_kernel(const float *__restrict__ w, float *__restrict__ wp, int OC, i
     if (c < C) tf32_split(__ldg(w + ((int64_t)oc * C + c) * taps + tap), h, l);
     wp[r * 2 * Cs + c] = h;
     wp[r * 2 * Cs + Cs + c] = l;
+}
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t S) {
+    __shared__ float tile[kSpC][kSpS + 1];
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    split_nchw_block<VEC>(x, xs, C, Cs, S, blockIdx.x, blockIdx.y, blockIdx.z, tile);
+}
+__global__ void __launch_bounds__(256)
+split_cl_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t positions) {
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    split_cl_elem(x, xs, C, Cs, positions, (int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+}
+__global__ void __launch_bounds__(256)
+pack_split_kernel(const float *__restrict__ w, float *__restrict__ wp, int OC, int C, int Cs, int taps) {
+    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    pack_split_elem(w, wp, OC, C, Cs, taps, (int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+}
+// The split-pack of OIHW weights and the split of x as one grid: npk CTAs
+// pack 256 weight elements each, nsp split x (NC(D)HW blocks of a
+// spx x spy x N grid, x fastest, or 256 channels-last elements each when
+// XM == 0). XM: 0 channels-last x, 1 NC(D)HW, 2 NC(D)HW with 16-byte loads.
+template <int XM>
+__global__ void __launch_bounds__(256)
+prep_split_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t S, int64_t positions,
+                  int spx, int spy, const float *__restrict__ w, float *__restrict__ wp, int OC, int taps, int npk,
+                  int nsp) {
+    __shared__ float tile[kSpC][kSpS + 1];
+    pdl_wait();   // dependents start when this grid completes
+    bool pack;
+    const int q = prep_block_index(blockIdx.x, npk, nsp, &pack);
+    if (pack) {
+        pack_split_elem(w, wp, OC, C, Cs, taps, (int64_t)q * 256 + threadIdx.x);
+    } else {
+        if (XM == 0)
+            split_cl_elem(x, xs, C, Cs, positions, (int64_t)q * 256 + threadIdx.x);
+        else
+            split_nchw_block<XM == 2>(x, xs, C, Cs, S, q % spx, (q / spx) % spy, q / (spx * spy), tile);
+    }
 }
 
 cudaError_t launch_split(const Problem &p, const void *x, void *xs, cudaStream_t s) {
@@ -1040,6 +1117,38 @@ cudaError_t launch_pack_tc_typed(const Problem &p, const void *w, void *wp, cuda
     return launch_pdl(pack_tc_kernel<T>, grid, dim3(256), 0, s, static_cast<const T *>(w), static_cast<T *>(wp),
                       p.OC, p.C, Cp, p.taps);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_prep_tc_typed(const Problem &p, const void *w, void *wp, const void *x, void *xc, cudaStream_t s) {
+    const int Cp = tc_cpad(p.C);
+    const int64_t S = p.in_vol;
+    const int64_t clx = (S + kClS - 1) / kClS, cly = (Cp + kClC - 1) / kClC;
+    const int64_t pky = (Cp + kPkC - 1) / kPkC, pkz = (p.taps + kPkT - 1) / kPkT;
+    const int64_t npk = (int64_t)p.OC * pky * pkz, nlay = clx * cly * p.N;
+    const int64_t total = npk + nlay;
+    if (total > 0x7FFFFFFF) return cudaErrorNotSupported;   // caller falls back to two launches
+    const bool vec = (S % 8 == 0) && ((uintptr_t)x % 16 == 0);
+    auto kern = vec ? prep_tc_kernel<T, true> : prep_tc_kernel<T, false>;
+    return launch_pdl(kern, dim3((unsigned)total), dim3(256), 0, s, static_cast<const T *>(x), static_cast<T *>(xc),
+                      p.C, Cp, S, (int)clx, (int)cly, static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.taps,
+                      (int)pky, (int)npk, (int)nlay);
+}
+
+cudaError_t launch_prep_split(const Problem &p, const void *w, void *wp, const void *x, void *xs, cudaStream_t s) {
+    const int Cs = tc_split_half(p.C);
+    const int64_t S = p.in_vol, positions = (int64_t)p.N * p.in_vol;
+    const int64_t spx = (S + kSpS - 1) / kSpS, spy = Cs / kSpC;
+    const int64_t nsp = p.cl ? (positions * Cs + 255) / 256 : spx * spy * p.N;
+    const int64_t npk = ((int64_t)p.taps * p.OC * Cs + 255) / 256;
+    const int64_t total = npk + nsp;
+    if (total > 0x7FFFFFFF) return cudaErrorNotSupported;   // caller falls back to two launches
+    const float *xf = static_cast<const float *>(x), *wf = static_cast<const float *>(w);
+    float *xo = static_cast<float *>(xs), *wo = static_cast<float *>(wp);
+    auto kern = p.cl ? prep_split_kernel<0>
+                     : (S % 4 == 0 && (uintptr_t)xf % 16 == 0) ? prep_split_kernel<2> : prep_split_kernel<1>;
+    return launch_pdl(kern, dim3((unsigned)total), dim3(256), 0, s, xf, xo, p.C, Cs, S, positions, (int)spx,
+                      (int)spy, wf, wo, p.OC, p.taps, (int)npk, (int)nsp);
 }
 
 }  // namespace
@@ -1094,5 +1203,16 @@ cudaError_t launch_pack_tc(const Problem &p, const void *w, void *wp, cudaStream
     if (p.dtype == GBCONV_BF16) return launch_pack_tc_typed<__nv_bfloat16>(p, w, wp, s);
     return launch_pack_tc_typed<__half>(p, w, wp, s);
 }
+
+cudaError_t launch_prep_tc(const Problem &p, const void *w, void *wp, const void *x, void *xc, cudaStream_t s) {
+    cudaError_t e;
+    if (p.dtype == GBCONV_F32) e = launch_prep_split(p, w, wp, x, xc, s);
+    else if (p.dtype == GBCONV_BF16) e = launch_prep_tc_typed<__nv_bfloat16>(p, w, wp, x, xc, s);
+    else e = launch_prep_tc_typed<__half>(p, w, wp, x, xc, s);
+    if (e != cudaErrorNotSupported) return e;
+    e = launch_pack_tc(p, w, wp, s);
+    return e == cudaSuccess ? launch_to_channels_last(p, x, xc, s) : e;
+}
+
 
 }  // namespace gbconv

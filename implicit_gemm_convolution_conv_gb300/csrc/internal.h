@@ -78,6 +78,9 @@ cudaError_t launch_pack_tc(const Problem &p, const void *w_oihw,
                            void *w_packed, cudaStream_t s);
 cudaError_t launch_to_channels_last(const Problem &p, const void *x,
                                     void *x_cl, cudaStream_t s);
+// Both of the above in one launch (OIHW weights, x not read in place).
+cudaError_t launch_prep_tc(const Problem &p, const void *w_oihw, void *w_packed,
+                           const void *x, void *x_cl, cudaStream_t s);
 cudaError_t launch_stem_tc(const Problem &p, const void *x, const void *w_oihw,
                            const float *b, void *y, cudaStream_t s);
 // Returns cudaErrorInvalidValue when the tensor maps cannot be encoded.
