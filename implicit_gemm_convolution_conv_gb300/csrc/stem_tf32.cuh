@@ -234,6 +234,14 @@ __device__ __forceinline__ void stem_load_halo(const CUtensorMap *tmX, const Ste
     tma_load_4d(dst, tmX, bar, s.ow0 * a.stride - a.pad - a.hd, s.oh0 * a.stride - a.pad, 0, s.n);
 }
 
+// The same box as an L2 prefetch, its start clamped to the image (a hint
+// needs no zero fill; column 0 keeps the 16-byte alignment).
+__device__ __forceinline__ void stem_prefetch_halo(const CUtensorMap *tmX, const StemTcArgs &a, int t) {
+    const StemTile s = stem_tile(a, t);
+    const int x0 = s.ow0 * a.stride - a.pad - a.hd, y0 = s.oh0 * a.stride - a.pad;
+    tma_prefetch_l2_4d(tmX, x0 > 0 ? x0 : 0, y0 > 0 ? y0 : 0, 0, s.n);
+}
+
 // Bias, the two halves of the accumulator, ReLU; one store per output
 // channel of this thread's pixel (y_px: its address in channel 0; the
 // channel stride is OH * OW).
@@ -311,6 +319,10 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         if (TMA) {
             prefetch_tmap(&tmX);
             prefetch_tmap(&tmY);
+            // The group's first two halos start towards L2 while the previous
+            // kernel finishes; the loads after the wait below read them there.
+            for (int k = 0; k < 2; ++k)
+                if (tile + k * tstep < tend) stem_prefetch_halo(&tmX, a, tile + k * tstep);
         }
     }
     if (tid < 32) {
