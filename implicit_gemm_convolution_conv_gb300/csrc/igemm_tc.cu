@@ -118,6 +118,8 @@ struct TcArgs {
     int pair_store;        // channels-last: 4-byte stores of channel pairs (OC even, y 4-byte aligned)
     int tma_store;         // staged chunks leave as TMA tensor stores (tmY valid)
     int single_tile;       // every CTA owns at most one tile: the staging tiles reuse the stage ring
+    int prefetch;          // L2 prefetch before the dependency wait: 1 x (read in place), 2 packed weights too
+    int in_w, in_h, in_d;  // input extents (prefetch boxes start inside them)
     uint32_t idesc;
     uint32_t tx_bytes;
     uint32_t tmem_cols;
@@ -192,6 +194,33 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
         if (a.tma_store) prefetch_tmap(&tmY);
+        // The first ring's worth of the first tile's boxes, for operands that
+        // no kernel of this call writes, start towards L2 while the previous
+        // kernel finishes (L2 is where the GPU's writes become coherent, so
+        // the loads after the wait cannot see stale data). Starts are
+        // clamped to the tensor: a hint needs no zero fill.
+        if (!TcElt<T>::kSplit && a.prefetch && (int)blockIdx.x < a.num_tiles) {
+            const TileCoord tc = tile_coord(a, blockIdx.x);
+            const int x0 = tc.ow0 * a.stride - a.pad, y0 = tc.oh0 * a.stride - a.pad,
+                      z0 = tc.od * a.stride - a.pad_d;
+            int cb = 0, tap = 0, kx = 0, ky = 0, kz = 0;
+            for (int it = 0; it < a.stages && it < a.ksteps; ++it) {
+                const int c0 = cb * TcElt<T>::kBlk;
+                if (a.prefetch & 2) tma_prefetch_l2_3d(&tmW, c0, tc.oc0, tap);
+                const int xs = x0 + kx > 0 ? x0 + kx : 0, ys = y0 + ky > 0 ? y0 + ky : 0,
+                          zs = z0 + kz > 0 ? z0 + kz : 0;
+                if ((a.prefetch & 1) && xs < a.in_w && ys < a.in_h && zs < a.in_d)
+                    tma_prefetch_l2_5d(&tmX, c0, xs, ys, zs, tc.n);
+                if (++cb == a.cblocks) {
+                    cb = 0;
+                    ++tap;
+                    if (++kx == a.k) {
+                        kx = 0;
+                        if (++ky == a.k) { ky = 0; ++kz; }
+                    }
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(slot_addr, a.tmem_cols);
@@ -945,6 +974,10 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.wait_limit_cycles = cyc > 9.0e18 ? (long long)9e18 : (long long)cyc;
 
     a.single_tile = single_tile ? 1 : 0;
+    // Only when x is read in place: behind the layout pass the weights alone
+    // measured no faster.
+    a.prefetch = tc_cl_direct(p) ? 1 | (p.w_layout == GBCONV_W_PACKED ? 2 : 0) : 0;
+    a.in_w = p.W; a.in_h = p.H; a.in_d = p.D;
     const size_t smem = smem_bytes(g, p, single_tile);
     auto kern = igemm_tc_kernel<T>;
     static std::atomic<uint64_t> attr_done{0};   // one bit per device
