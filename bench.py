@@ -559,8 +559,10 @@ def cpu_baseline(L, inp, budget_s=10.0):
 
 
 # ----------------------------------------------------------- reference
-# Work per reference-arm step: layers above it are timed on a seeded sample
-# of outputs so that the default K and W stay within minutes on the host.
+# Reference-arm steps: layers up to REF_WHOLE_FLOP run whole; larger ones
+# time a seeded sample of about REF_STEP_FLOP of their outputs per step, so
+# that the default K and W stay within minutes on the host.
+REF_WHOLE_FLOP = 5e9
 REF_STEP_FLOP = 2e9
 
 
@@ -573,7 +575,7 @@ def run_reference(args):
     import oracle
     threads = oracle.threads()
     total = int(np.prod(L.y_shape()))
-    if L.flops() <= REF_STEP_FLOP or L.pool:
+    if L.flops() <= REF_WHOLE_FLOP or L.pool:
         # a step is one whole-layer oracle call
         step = lambda: oracle_layer(oracle, L, inp)
         step_flop, sample = L.flops(), f"whole layer per step, {args.steps} steps"

@@ -56,6 +56,7 @@ def test_reference_arm_other_workload_keeps_its_config():
     assert d["impl"] == "reference"
     assert d["config"]["workload"] == "conv2d_f32_16x64x12x80_oc128_k3p1s1_relu"
     assert d["value"] > 0
+    assert d["cpu_baseline"]["sample"].startswith("whole layer")   # 2.27 GFLOP: whole calls
 
 
 def test_reference_arm_samples_the_large_layers():
