@@ -382,6 +382,8 @@ def run_ours(args):
             "clocks": clk.summary(),
             "wall_s_timed_region": round(t_wall, 4),
             "latency_us_isolated_call": round(statistics.median(iso) * 1e3, 3),
+            "latency_us_isolated_call_p10": quantile_us(iso, 0.1),
+            "latency_us_isolated_call_p90": quantile_us(iso, 0.9),
         }
     barrier()
 
@@ -449,6 +451,16 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def quantile_us(ms, f):
+    """The f-quantile (linear interpolation between order statistics) of
+    event times given in ms, in us."""
+    q = sorted(ms)
+    i = f * (len(q) - 1)
+    lo = int(i)
+    hi = min(lo + 1, len(q) - 1)
+    return round((q[lo] + (q[hi] - q[lo]) * (i - lo)) * 1e3, 3)
+
+
 def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
     """TFLOP/s, GB/s and roofline fraction of every layer shape: average
     call time of back-to-back calls on rotated buffers (graph replay), with
@@ -513,6 +525,8 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
                 "l2": rot.l2_note,
                 "us_per_call_l2_resident": round(s_warm * 1e6, 3),
                 "us_isolated_call_median": round(statistics.median(iso) * 1e3, 3),
+                "us_isolated_call_p10": quantile_us(iso, 0.1),
+                "us_isolated_call_p90": quantile_us(iso, 0.9),
             }
             del conv, rot, warm_rot, gs, gw
         out.append(rec)
