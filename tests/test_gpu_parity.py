@@ -89,6 +89,22 @@ def test_layer2_on_tensor_cores_full_output():
     assert_close(L.dtype, y, reference(inp), L.name)
 
 
+@pytest.mark.parametrize("OC,W", [(32, 640), (128, 640), (32, 638)])
+def test_stem_tensor_cores_many_tiles_per_group(OC, W):
+    """Four 640-row images through the tensor-core stem: 3,200 tiles, so
+    every group runs five or more tiles and its two halo buffers are reused
+    (barrier phases past the first flip). OC 32 keeps the pixel operand in
+    TMEM with four groups, OC 128 in shared memory with two; W = 638 (OW not
+    a multiple of 4) takes the plain-load path. Every output is checked."""
+    L = synthetic.Layer(f"stem_many_tiles_oc{OC}_w{W}", N=4, C=3, H=640, W=W, OC=OC, k=3, pad=1,
+                        stride=2, dtype="f32", relu=True, x_dist="u01", w_dist="he", b_dist="u01_1",
+                        seed=77 + OC + W)
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp, algo=A_DTC)
+    assert conv.algo == A_DTC
+    assert_close(L.dtype, y, reference(inp), L.name)
+
+
 @pytest.mark.parametrize("idx,dtype", [(4, "f16"), (5, "f16"), (4, "bf16")])
 def test_layer_sampled_output(idx, dtype):
     L = synthetic.layer(idx, dtype=dtype)
