@@ -5,6 +5,7 @@
 // uninitialised-activation bug case): every field is checked, unknown enum
 // values are rejected, and nothing is launched for a rejected call.
 #include <cstring>
+#include <initializer_list>
 
 #include "internal.h"
 
@@ -19,6 +20,22 @@ int64_t out_extent(int64_t in, int k, int pad, int stride) {
 }
 
 bool in_range(int v, int lo, int hi) { return v >= lo && v <= hi; }
+
+// a * b when it is at most `limit` (a, b >= 0), else -1: element counts are
+// formed without signed overflow, so a huge shape cannot wrap past the limit.
+int64_t mul_capped(int64_t a, int64_t b, int64_t limit) {
+    if (a < 0 || b < 0) return -1;
+    if (b != 0 && a > limit / b) return -1;
+    return a * b;
+}
+int64_t elems_capped(std::initializer_list<int64_t> factors, int64_t limit) {
+    int64_t n = 1;
+    for (int64_t f : factors) {
+        n = mul_capped(n, f, limit);
+        if (n < 0) return -1;
+    }
+    return n;
+}
 
 // Structural validation: shapes and enums only (no pointers).
 gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
@@ -71,12 +88,10 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     q.YH = pool ? q.OH / 2 : q.OH;
     q.YW = pool ? q.OW / 2 : q.OW;
     if (q.YH <= 0 || q.YW <= 0) return GBCONV_ERR_SHAPE;
-    q.x_elems = (int64_t)q.N * q.C * q.in_vol;
-    q.w_elems = (int64_t)q.OC * q.C * q.taps;
-    q.y_elems = (int64_t)q.N * q.OC * q.OD * q.YH * q.YW;
-    if (q.x_elems > GBCONV_MAX_ELEMS || q.w_elems > GBCONV_MAX_ELEMS ||
-        q.y_elems > GBCONV_MAX_ELEMS)
-        return GBCONV_ERR_SHAPE;
+    q.x_elems = elems_capped({q.N, q.C, q.D, q.H, q.W}, GBCONV_MAX_ELEMS);
+    q.w_elems = elems_capped({q.OC, q.C, q.taps}, GBCONV_MAX_ELEMS);
+    q.y_elems = elems_capped({q.N, q.OC, q.OD, q.YH, q.YW}, GBCONV_MAX_ELEMS);
+    if (q.x_elems < 0 || q.w_elems < 0 || q.y_elems < 0) return GBCONV_ERR_SHAPE;
     q.dtype = d->dtype; q.act = d->act; q.w_layout = d->w_layout;
     q.elt = d->dtype == GBCONV_F32 ? 4 : 2;
 

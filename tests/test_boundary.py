@@ -89,6 +89,30 @@ BAD = [
 ]
 
 
+@pytest.mark.parametrize("dims,ndim", [
+    ((65535,) * 6, 3),                                 # N C D H W OC: 65535^5 wraps int64
+    ((65535, 65535, 1, 65535, 65535, 65535), 2),       # x: 65535^4 > 2^63
+    ((65535, 1, 65535, 65535, 65535, 1), 3),
+    ((1, 65535, 65535, 65535, 65535, 1), 3),
+])
+def test_element_counts_that_overflow_int64_are_rejected(dims, ndim):
+    # Element counts are formed with a capped product, so a shape whose
+    # count exceeds int64 cannot wrap below the element limit and pass.
+    N, C, D, H, W, OC = dims
+    d = gb.make_desc(N, C, H, W, OC, 3, 1, 1, D=D)
+    assert gb.workspace_size(d, ndim)[0] == gb.ERR_SHAPE
+    assert gb.select_algo(d, ndim)[0] == gb.ERR_SHAPE
+    assert gb.output_shape(d, ndim)[0] == gb.ERR_SHAPE
+    fwd = gb.conv3d_fwd if ndim == 3 else gb.conv2d_fwd
+    assert fwd(d, FAKE, FAKE, FAKE, FAKE * 2, 0) == gb.ERR_SHAPE
+
+
+def test_element_limit_is_inclusive():
+    # 4096^3 = 2^36 elements of x (the limit itself) is a valid shape
+    d = gb.make_desc(4096, 4096, 64, 64, 1, 3, 1, 1)
+    assert gb.select_algo(d, 2)[0] == gb.OK
+
+
 @pytest.mark.parametrize("kw,status", BAD)
 def test_invalid_desc_rejected_before_cuda(kw, status):
     d = _desc(**kw)
