@@ -37,6 +37,18 @@ int64_t elems_capped(std::initializer_list<int64_t> factors, int64_t limit) {
     return n;
 }
 
+// The tensor-core path for this problem, within CUDA's grid limits: the
+// element-wise split of channels-last fp32 x runs one 256-thread CTA per 256
+// elements of its [N][S][Cs] half, in a 1-D grid.
+bool tc_ok(const Problem &q) {
+    if (!tc_supported(q)) return false;
+    if (q.dtype == GBCONV_F32 && q.cl) {
+        const int64_t n = (int64_t)q.N * q.in_vol * tc_split_half(q.C);
+        if ((n + 255) / 256 > 0x7FFFFFFF) return false;
+    }
+    return true;
+}
+
 // Structural validation: shapes and enums only (no pointers).
 gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     if (!d) return GBCONV_ERR_NULL;
@@ -101,8 +113,8 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
     int algo = d->algo;
     if (algo == GBCONV_ALGO_AUTO && q.cl) {
         // Channels-last: the implicit GEMMs only (the direct kernels read NCHW).
-        algo = ((q.dtype == GBCONV_F32 || tc_cl_direct(q)) && tc_supported(q)) ? GBCONV_ALGO_IGEMM_TC
-                                                                             : GBCONV_ALGO_IGEMM_FFMA;
+        algo = ((q.dtype == GBCONV_F32 || tc_cl_direct(q)) && tc_ok(q)) ? GBCONV_ALGO_IGEMM_TC
+                                                                       : GBCONV_ALGO_IGEMM_FFMA;
     } else if (algo == GBCONV_ALGO_AUTO) {
         // fp32 3x3 stems of 16+ output channels: the tensor-core stem
         // (measured faster than the CUDA-core stem from 16 to 128 channels
@@ -113,15 +125,14 @@ gbconv_status build_problem(const gbconv_desc *d, int ndim, Problem *p) {
             algo = GBCONV_ALGO_DIRECT_TC;
         else if ((int64_t)q.C * q.taps <= 64 && direct_supported(q))
             algo = GBCONV_ALGO_DIRECT;
-        else if (tc_supported(q))
+        else if (tc_ok(q))
             algo = GBCONV_ALGO_IGEMM_TC;       // fp32: three TF32 products
-
         else
             algo = GBCONV_ALGO_IGEMM_FFMA;
     }
     q.algo = algo;
     if (algo == GBCONV_ALGO_DIRECT && !direct_supported(q)) return GBCONV_ERR_ALGO;
-    if (algo == GBCONV_ALGO_IGEMM_TC && !tc_supported(q)) return GBCONV_ERR_ALGO;
+    if (algo == GBCONV_ALGO_IGEMM_TC && !tc_ok(q)) return GBCONV_ERR_ALGO;
     if (algo == GBCONV_ALGO_DIRECT_TC && !stem_tc_supported(q)) return GBCONV_ERR_ALGO;
     if (q.cl && !(algo == GBCONV_ALGO_IGEMM_FFMA ||
                   (algo == GBCONV_ALGO_IGEMM_TC && (tc_cl_direct(q) || q.dtype == GBCONV_F32))))

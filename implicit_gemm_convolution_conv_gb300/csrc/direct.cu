@@ -200,7 +200,12 @@ cudaError_t launch_typed(const Problem &p, const DirectArgs &a, cudaStream_t st)
 bool direct_supported(const Problem &p) {
     const size_t wide = direct_smem_bytes<4, 64, 32, 4, 16>(p);
     const size_t narrow = direct_smem_bytes<8, 32, 8, 2, 8>(p);
-    return (p.OC >= 16 ? wide : narrow) <= kDirectSmemLimit;
+    if ((p.OC >= 16 ? wide : narrow) > kDirectSmemLimit) return false;
+    if (stem_supported(p)) return true;   // persistent kernel, 1-D grid
+    // The tile kernel's grid z is images x frames x output-channel blocks
+    // (32 channels wide, 8 narrow); CUDA caps it at 65535.
+    const int ocb = p.OC >= 16 ? 32 : 8;
+    return (int64_t)p.N * p.OD * ((p.OC + ocb - 1) / ocb) <= 65535;
 }
 
 cudaError_t launch_direct(const Problem &p, const void *x, const void *w,

@@ -107,6 +107,17 @@ def test_element_counts_that_overflow_int64_are_rejected(dims, ndim):
     assert fwd(d, FAKE, FAKE, FAKE, FAKE * 2, 0) == gb.ERR_SHAPE
 
 
+def test_direct_tile_kernel_grid_limit():
+    # The tile kernel's grid z is images x frames x output-channel blocks,
+    # at most 65535: beyond it DIRECT is refused and AUTO picks a GEMM.
+    big = gb.make_desc(40000, 1, 8, 8, 64, 5, 2, 1, algo=gb.ALGO_DIRECT)   # 40000 x 2 blocks
+    assert gb.select_algo(big, 2)[0] == gb.ERR_ALGO
+    st, algo = gb.select_algo(gb.make_desc(40000, 1, 8, 8, 64, 5, 2, 1), 2)
+    assert st == gb.OK and algo != gb.ALGO_DIRECT
+    ok = gb.make_desc(1000, 1, 8, 8, 64, 5, 2, 1, algo=gb.ALGO_DIRECT)
+    assert gb.select_algo(ok, 2) == (gb.OK, gb.ALGO_DIRECT)
+
+
 def test_element_limit_is_inclusive():
     # 4096^3 = 2^36 elements of x (the limit itself) is a valid shape
     d = gb.make_desc(4096, 4096, 64, 64, 1, 3, 1, 1)
