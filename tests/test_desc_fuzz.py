@@ -4,7 +4,8 @@ Every field of `gbconv_desc` is drawn from a mix of valid values, boundary
 values (0, 1, the limits and one past them) and wild ones (negative, 2^31 - 1),
 and each descriptor goes through the host-only queries. The library must
 answer every one with a status code, never crash, and answer consistently:
-- the status of `select_algo`, `workspace_size` and `output_shape` is the same;
+- the status of `select_algo`, `workspace_size`, `output_shape` and
+  `weight_packed_size` is the same;
 - an accepted descriptor has positive output extents within the limits, a
   resolved algorithm (never AUTO), and its output element count within
   GBCONV_MAX_ELEMS;
@@ -69,7 +70,8 @@ def test_fuzzed_descriptors_get_consistent_answers(seed):
         st_a, algo = gb.select_algo(d, ndim)
         st_w, ws = gb.workspace_size(d, ndim)
         st_o, (od, oh, ow) = gb.output_shape(d, ndim)
-        assert st_a == st_w == st_o, (ndim, f, st_a, st_w, st_o)
+        st_p, packed = gb.weight_packed_size(d, ndim)
+        assert st_a == st_w == st_o == st_p, (ndim, f, st_a, st_w, st_o, st_p)
         if st_a != gb.OK:
             # the forward call rejects it the same way, before any CUDA call
             # (fake, aligned, non-overlapping pointers; nothing is read)
@@ -81,7 +83,7 @@ def test_fuzzed_descriptors_get_consistent_answers(seed):
         assert algo != gb.ALGO_AUTO and algo in (gb.ALGO_DIRECT, gb.ALGO_IGEMM_FFMA,
                                                  gb.ALGO_IGEMM_TC, gb.ALGO_DIRECT_TC)
         assert 1 <= oh <= MAX_DIM + 2 * MAX_K and 1 <= ow <= MAX_DIM + 2 * MAX_K and od >= 1
-        assert ws >= 0
+        assert ws >= 0 and packed > 0
         assert f["N"] * f["OC"] * od * oh * ow <= MAX_ELEMS
         assert f["N"] * f["C"] * f["D"] * f["H"] * f["W"] <= MAX_ELEMS
         forced = _desc(dict(f, algo=algo))
