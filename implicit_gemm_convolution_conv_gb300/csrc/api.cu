@@ -180,9 +180,11 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
         if (!d->workspace || d->workspace_bytes < ws.total) return GBCONV_ERR_WORKSPACE;
         if (!aligned(d->workspace, 256)) return GBCONV_ERR_WORKSPACE;
     }
-    if (overlap(y, yb, x, xb) || overlap(y, yb, w, wb) ||
-        overlap(y, yb, b, b ? (size_t)p.OC * 4 : 0) ||
-        overlap(y, yb, d->workspace, ws.total))
+    // The kernels write y and the workspace while they read x, w and b.
+    const size_t bb = b ? (size_t)p.OC * 4 : 0;
+    if (overlap(y, yb, x, xb) || overlap(y, yb, w, wb) || overlap(y, yb, b, bb) ||
+        overlap(y, yb, d->workspace, ws.total) || overlap(d->workspace, ws.total, x, xb) ||
+        overlap(d->workspace, ws.total, w, wb) || overlap(d->workspace, ws.total, b, bb))
         return GBCONV_ERR_OVERLAP;
     st = device_check();
     if (st != GBCONV_OK) return st;

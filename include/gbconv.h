@@ -68,7 +68,7 @@ typedef enum gbconv_status {
     GBCONV_ERR_TIMEOUT = 9,            /* a bounded device-side wait ran out */
     GBCONV_ERR_ALGO = 10,              /* unknown algorithm, or the forced one cannot run this shape */
     GBCONV_ERR_LAYOUT = 11,            /* unknown weight layout */
-    GBCONV_ERR_OVERLAP = 12,           /* y overlaps x, w, b or the workspace */
+    GBCONV_ERR_OVERLAP = 12,           /* y overlaps x, w, b or the workspace, or the workspace x, w or b */
     GBCONV_ERR_CUDA = 13,              /* another CUDA runtime/driver call failed */
     GBCONV_ERR_RESERVED = 14,          /* a reserved flag bit is set, or an unknown frame-padding mode */
     GBCONV_ERR_TOO_LARGE = 15          /* gbconv_conv_fwd_noalloc: scratch need exceeds its fixed array */

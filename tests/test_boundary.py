@@ -169,6 +169,19 @@ def test_workspace_checks():
     assert gb.weight_packed_size(d, 2) == (gb.OK, w_pk)
 
 
+def test_workspace_overlapping_an_input_is_rejected():
+    # The layout pass and the weight pack write the workspace while x, w and
+    # b are read: a workspace over any of them is refused before any CUDA call.
+    L = synthetic.LAYERS[4]
+    d = gb.make_desc(L.N, L.C, L.H, L.W, L.OC, L.k, L.pad, L.stride, dtype=gb.F16)
+    need = gb.workspace_size(d, 2)[1]
+    x, w, b, y = FAKE, FAKE * 64, FAKE * 96, FAKE * 128      # x spans 8.4 MB from 1 MiB
+    d.workspace_bytes = need
+    for ws in (x + 4096 * 256, w, b - 256):                   # inside x, at w, over b
+        d.workspace = ws
+        assert gb.conv2d_fwd(d, x, w, b, y, 0) == gb.ERR_OVERLAP, ws
+
+
 @pytest.mark.skipif(HAVE_GPU, reason="this check needs a machine without a GPU")
 def test_valid_desc_reaches_device_check_without_gpu():
     """A fully valid call on a machine without a GPU returns
