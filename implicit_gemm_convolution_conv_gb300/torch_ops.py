@@ -53,6 +53,36 @@ def _desc(x, OC, k, stride, pad, relu, algo, w_layout, tpad=0, pool=False,
     return d, nsp
 
 
+def check_tensors(x, w, b=None, channels_last=False, require_cuda=True):
+    """The checks a raw-pointer ABI cannot make: x, w and b are contiguous
+    tensors on one CUDA device, w has x's dtype and the shape [OC, C, k, k]
+    (conv2d) or [OC, C, k, k, k] (conv3d) with C = x's channels, and b is
+    fp32 with OC elements. Raises TypeError or ValueError; returns (OC, k)."""
+    for name, t in (("x", x), ("w", w)) + ((("b", b),) if b is not None else ()):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if require_cuda and not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != x.device:
+            raise ValueError(f"{name} is on {t.device}, x on {x.device}")
+    if x.dtype not in CODE_OF:
+        raise ValueError(f"x has dtype {x.dtype}; float32, float16 or bfloat16 expected")
+    if x.dim() not in (4, 5):
+        raise ValueError("x must be 4-D (conv2d) or 5-D (conv3d)")
+    if w.dtype != x.dtype:
+        raise ValueError(f"w has dtype {w.dtype}, x {x.dtype}")
+    C = x.shape[-1] if channels_last else x.shape[1]
+    nsp = x.dim() - 2
+    if w.dim() != x.dim() or w.shape[1] != C or len(set(w.shape[2:])) != 1:
+        raise ValueError(f"w has shape {tuple(w.shape)}; [OC, {C}] + {nsp} equal kernel sizes expected")
+    OC, k = w.shape[0], w.shape[-1]
+    if b is not None and (b.dtype != torch.float32 or b.numel() != OC):
+        raise ValueError(f"b must be float32 with {OC} elements")
+    return OC, k
+
+
 def output_tensor(x, OC, k, stride, pad):
     sp = [(n + 2 * pad - k) // stride + 1 for n in x.shape[2:]]
     return torch.empty([x.shape[0], OC] + sp, dtype=x.dtype, device=x.device)
@@ -69,8 +99,8 @@ class Conv:
     def __init__(self, x, w, b=None, stride=1, pad=0, relu=False,
                  algo=ALGO_AUTO, prepack=False, out=None, workspace=None, tpad=0,
                  pool=False, channels_last=False):
+        OC, k = check_tensors(x, w, b, channels_last)
         self.x, self.b = x, b
-        OC, k = w.shape[0], w.shape[-1]
         layout = W_PACKED if prepack else W_OIHW
         self.channels_last = channels_last
         self.desc, self.nsp = _desc(x, OC, k, stride, pad, relu, algo, layout, tpad, pool,
@@ -92,15 +122,21 @@ class Conv:
             if workspace is None:
                 raw = torch.empty(ws + 256, dtype=torch.uint8, device=x.device)
                 workspace = _aligned_view(raw, ws)
+            elif not (workspace.is_contiguous() and workspace.device == x.device):
+                raise ValueError("workspace must be a contiguous tensor on x's device")
             self.desc.workspace = workspace.data_ptr()
-            self.desc.workspace_bytes = ws
+            # the tensor's real size: the library refuses one that is too small
+            self.desc.workspace_bytes = workspace.numel() * workspace.element_size()
         self.workspace = workspace
+        st, (od, oh, ow) = output_shape(self.desc, self.nsp)
+        check(st)
+        sp = [oh, ow] if self.nsp == 2 else [od, oh, ow]
+        shape = [x.shape[0]] + sp + [OC] if channels_last else [x.shape[0], OC] + sp
         if out is None:
-            st, (od, oh, ow) = output_shape(self.desc, self.nsp)
-            check(st)
-            sp = [oh, ow] if self.nsp == 2 else [od, oh, ow]
-            shape = [x.shape[0]] + sp + [OC] if channels_last else [x.shape[0], OC] + sp
             out = torch.empty(shape, dtype=x.dtype, device=x.device)
+        elif (list(out.shape) != shape or out.dtype != x.dtype or out.device != x.device or
+              not out.is_contiguous()):
+            raise ValueError(f"out must be a contiguous {x.dtype} tensor of shape {shape} on {x.device}")
         self.y = out
         self._fn = conv2d_fwd if self.nsp == 2 else conv3d_fwd
 
@@ -113,6 +149,9 @@ class Conv:
         return c
 
     def __call__(self, x=None, stream=None):
+        if x is not None and (x.shape != self.x.shape or x.dtype != self.x.dtype or
+                              x.device != self.x.device or not x.is_contiguous()):
+            raise ValueError("x must match the prepared input's shape, dtype and device, contiguous")
         st = self._fn(self.desc, self.x if x is None else x, self.w, self.b,
                       self.y, stream)
         if st != 0:

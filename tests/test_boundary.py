@@ -323,3 +323,31 @@ def test_status_and_algo_names():
         "auto", "direct", "igemm_ffma", "igemm_tc", "direct_tc"]
     assert gb.set_wait_limit_ns(0) == gb.ERR_SHAPE
     assert gb.set_wait_limit_ns(2_000_000_000) == gb.OK
+
+
+def test_torch_front_end_checks_what_pointers_cannot_say():
+    # The C ABI takes raw pointers; the torch front end checks devices,
+    # contiguity, dtypes and the weight/bias shapes before any call.
+    from implicit_gemm_convolution_conv_gb300.torch_ops import Conv, check_tensors
+    x, w, b = torch.zeros(1, 3, 8, 8), torch.zeros(4, 3, 3, 3), torch.zeros(4)
+    assert check_tensors(x, w, b, require_cuda=False) == (4, 3)
+    assert check_tensors(torch.zeros(1, 8, 8, 3), w, None, channels_last=True, require_cuda=False) == (4, 3)
+    assert check_tensors(torch.zeros(1, 3, 4, 8, 8), torch.zeros(4, 3, 3, 3, 3), None,
+                         require_cuda=False) == (4, 3)
+    bad = [
+        (x, torch.zeros(4, 2, 3, 3), b),             # channel count differs from x
+        (x, torch.zeros(4, 3, 3, 5), b),             # non-square kernel
+        (x, torch.zeros(4, 3, 3, 3, 3), b),          # conv3d weights for a 4-D x
+        (x, w.half(), b),                            # dtype differs from x
+        (x, w, torch.zeros(5)),                      # bias length
+        (x, w, torch.zeros(4, dtype=torch.float64)), # bias dtype
+        (x.transpose(2, 3), w, b),                   # non-contiguous x
+        (x.long(), w.long(), b),                     # unsupported dtype
+    ]
+    for args in bad:
+        with pytest.raises(ValueError):
+            check_tensors(*args, require_cuda=False)
+    with pytest.raises(TypeError):
+        check_tensors(x, w.numpy(), b, require_cuda=False)
+    with pytest.raises(ValueError, match="CUDA"):
+        Conv(x, w, b)                                # CPU tensors: there is no CPU path
