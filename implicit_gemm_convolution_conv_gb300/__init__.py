@@ -10,6 +10,8 @@ the import fails.
 import ctypes
 import os
 
+import numpy as np
+
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgbconv.so")
 
@@ -112,6 +114,12 @@ def make_desc(N, C, H, W, OC, k, pad=0, stride=1, D=1, dtype=F32,
               channels_last=False):
     if isinstance(dtype, str):
         dtype = DTYPES[dtype]
+    ints = dict(N=N, C=C, H=H, W=W, OC=OC, k=k, pad=pad, stride=stride, D=D, dtype=dtype, act=act,
+                w_layout=w_layout, algo=algo, flags=flags, tpad=tpad)
+    for name, v in ints.items():
+        # the fields are C ints: a wider value would wrap silently in ctypes
+        if not isinstance(v, (int, np.integer)) or not -2**31 <= int(v) < 2**31:
+            raise ValueError(f"{name}={v!r} is not a 32-bit integer")
     d = Desc()
     d.N, d.C, d.D, d.H, d.W = N, C, D, H, W
     d.OC, d.k, d.pad, d.stride = OC, k, pad, stride

@@ -351,3 +351,12 @@ def test_torch_front_end_checks_what_pointers_cannot_say():
         check_tensors(x, w.numpy(), b, require_cuda=False)
     with pytest.raises(ValueError, match="CUDA"):
         Conv(x, w, b)                                # CPU tensors: there is no CPU path
+
+
+def test_make_desc_refuses_values_wider_than_a_c_int():
+    # ctypes would wrap 2^32 + 1 to 1 without a word; the binding refuses it
+    for kw in (dict(N=2**32 + 1), dict(C=-2**31 - 1), dict(OC=2**40)):
+        args = dict(N=1, C=3, H=8, W=8, OC=4, k=3, pad=1, stride=1)
+        args.update(kw)
+        with pytest.raises(ValueError):
+            gb.make_desc(**args)
