@@ -1,13 +1,16 @@
 """Benchmark of the forward-convolution library on GB300.
 
-Default workload: the detection-stem layer (conv2d fp32, N=1, IC=3, 640x640,
-OC=32, k=3, pad 1, stride 2, bias + ReLU): one step is one forward call
-through the C ABI (gbconv_conv2d_fwd) with inputs resident in HBM. L2 (129
-MB) is larger than the layer's 18 MB working set, so a 256 MiB buffer is
-written between timed steps, outside the timed events. The line also carries
-the per-layer TFLOP/s, GB/s and roofline fraction of all five layer shapes,
-an end-to-end number with host buffers, and the CPU oracle timed on the host
-cores as a baseline.
+Default workload: the video-VAE Convolution3D layer (conv3d, fp16 storage,
+fp32 accumulation, N=1, IC=128, 5 frames of 128x240, OC=128, k=3, pad 1,
+stride 1, bias; NCDHW x, OIDHW weights packed inside the call), the largest
+of the five layer shapes and the one the pages time (SeedVR2's VAE decoder,
+git.erdda.com/Tencent/ncnn/discussions/7001). One step is one forward call
+through the C ABI (gbconv_conv3d_fwd) with inputs resident in HBM; steps
+rotate over copies of x and y larger than L2 (129 MB), so no step finds its
+operands there. The line also carries the per-layer TFLOP/s, GB/s and
+roofline fraction of all five layer shapes (`--workload` picks any of them
+as the headline), an end-to-end number with host buffers, and the CPU oracle
+timed on the host cores as a baseline.
 
 Multi-GPU: each rank runs an independent replica of the workload on its own
 GPU (the layer is one problem; no data exchange), barrier + synchronize
@@ -56,7 +59,7 @@ def workload_layer(name):
     idx, kw, suffix = VARIANTS[name]
     base = synthetic.LAYERS[idx]
     return dataclasses.replace(base, name=base.name + suffix, **kw)
-DEFAULT_WORKLOAD = "detection_stem"
+DEFAULT_WORKLOAD = "video_vae_conv3d_f16"
 
 
 def device_x(L, inp):
@@ -115,7 +118,10 @@ def job_tflops(flop_per_step, steps, world, total_ms):
 
 # --------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 100 ms while running."""
+    """nvidia-smi clock/throttle samples every 100 ms while running. It runs
+    over the whole bench (the timed region of a short run lasts milliseconds,
+    below the sampler's period); `summary` reports the samples taken while
+    the GPU drew power well above idle, i.e. under this run's load."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,"
          "clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,"
@@ -151,8 +157,8 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    def summary(self, note=None):
+        rows, mx = [], None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         for ln in self.lines:
@@ -160,16 +166,24 @@ class ClockSampler:
             if len(f) < 8:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                sm, mx, pw = float(f[1]), float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            rows.append((sm, pw, {n for n, v in zip(names, f[4:8]) if v.lower() == "active"}))
+        # under load: power at least idle + 30% of the range seen
+        if rows:
+            p_lo, p_hi = min(r[1] for r in rows), max(r[1] for r in rows)
+            load = [r for r in rows if r[1] >= p_lo + 0.3 * (p_hi - p_lo)] or rows
+        else:
+            load = []
+        reasons = set().union(*[r[2] for r in load]) if load else set()
+        out = {"sm_mhz": statistics.median(r[0] for r in load) if load else None,
+               "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(rows), "samples_under_load": len(load),
+               "power_w_max": max((r[1] for r in rows), default=None)}
+        if note:
+            out["window"] = note
+        return out
 
 
 # --------------------------------------------------------- traffic table
@@ -281,6 +295,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         return [e0.elapsed_time(e1) for e0, e1 in evs]
 
+    clk = ClockSampler(local).__enter__()
     L = workload_layer(args.workload)
     inp = synthetic.make_inputs(L)
     x, w = to_device(device_x(L, inp), L.dtype, dev), to_device(inp.w, L.dtype, dev)
@@ -298,17 +313,19 @@ def run_ours(args):
         rot.eager_step()
     barrier()
     graphs = rot.graphs(args.steps)
+    # each distinct graph once, untimed: its first replay uploads it
+    for g in {id(g): g for g in graphs}.values():
+        g.replay()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier()
-        t_wall = time.perf_counter()
-        e0.record(stream)
-        for g in graphs:
-            g.replay()
-        e1.record(stream)
-        barrier()
-        t_wall = time.perf_counter() - t_wall
+    barrier()
+    t_wall = time.perf_counter()
+    e0.record(stream)
+    for g in graphs:
+        g.replay()
+    e1.record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
     total_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     flops = L.flops()
     value = job_tflops(flops, args.steps, world, total_ms)
@@ -379,7 +396,6 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "roofline": roof,
             "gpu_launches": launches * args.steps,
-            "clocks": clk.summary(),
             "wall_s_timed_region": round(t_wall, 4),
             "latency_us_isolated_call": round(statistics.median(iso) * 1e3, 3),
             "latency_us_isolated_call_p10": quantile_us(iso, 0.1),
@@ -392,8 +408,12 @@ def run_ours(args):
         # the timed region, through the same C-ABI call. Consecutive steps
         # rotate over three streams, each with its own device buffers (x, w,
         # b, y, workspace), so one step's D2H overlaps the next steps' H2D
-        # and calls (more streams measured no faster); every step still
-        # copies all its inputs in and its output out.
+        # and calls; every step still copies all its inputs in and its output
+        # out. Each stream's step (three copies in, the call, one copy out)
+        # is captured once into a CUDA graph and replayed, so the host issues
+        # one launch per step instead of five calls (page 2,
+        # m.demingchina.com/news/41165: capture and replay hides the host's
+        # per-call launch cost).
         hx = torch.from_numpy(np.ascontiguousarray(device_x(L, inp))).pin_memory()
         hw = torch.from_numpy(np.ascontiguousarray(inp.w)).pin_memory()
         hb = torch.from_numpy(inp.b).pin_memory()
@@ -409,15 +429,25 @@ def run_ours(args):
             hyj = torch.empty(cj.y.shape, dtype=cj.y.dtype).pin_memory()
             pipes.append((torch.cuda.Stream(), xj, wj, bj, cj, hyj))
         torch.cuda.synchronize()
-
-        def e2e_step(i):
-            sj, xj, wj, bj, cj, hyj = pipes[i % n_pipe]
-            with torch.cuda.stream(sj):
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        step_graphs = []
+        for sj, xj, wj, bj, cj, hyj in pipes:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
                 xj.copy_(hx, non_blocking=True)
                 wj.copy_(hw, non_blocking=True)
                 bj.copy_(hb, non_blocking=True)
                 cj()
                 hyj.copy_(cj.y, non_blocking=True)
+            step_graphs.append(g)
+        torch.cuda.current_stream().wait_stream(cap)
+        torch.cuda.synchronize()
+
+        def e2e_step(i):
+            sj = pipes[i % n_pipe][0]
+            with torch.cuda.stream(sj):
+                step_graphs[i % n_pipe].replay()
         for i in range(3 * n_pipe):
             e2e_step(i)
         torch.cuda.synchronize()
@@ -439,13 +469,19 @@ def run_ours(args):
                        hw.numel() * hw.element_size() + hb.numel() * 4,
                        "d2h_bytes_per_step": hy.numel() * hy.element_size(),
                        "ms_per_step": round(e2e_ms, 5),
-                       "streams": n_pipe}
+                       "streams": n_pipe,
+                       "issue": "one CUDA graph per stream: H2D x, w, b; the C-ABI call; D2H y"}
         if not args.skip_layers:
             line["per_layer"] = per_layer(gb, Conv, to_device, torch, dev,
                                           timed_calls, pk, sms)
+        clk.__exit__()
+        line["clocks"] = clk.summary("whole bench run: warm-up, timed steps, isolated calls, "
+                                     "end-to-end and per-layer timing (samples every 100 ms)")
         if not args.skip_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(L, inp, budget_s=args.cpu_seconds)
         print(json.dumps(line), flush=True)
+    else:
+        clk.__exit__()
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -482,7 +518,6 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
         t_c = L.flops() / (pc * 1e12)
         t_m = L.compulsory_bytes() / (pk["hbm_gbs"] * 1e9)
         t_ideal = max(t_c, t_m)
-        t_ideal_335 = max(t_c, L.compulsory_bytes() / 3.35e12)
         for prepack in (False, True):
             conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack, tpad=L.tpad, pool=L.pool,
                         channels_last=L.cl)
@@ -491,6 +526,8 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
             for _ in range(3):
                 rot.eager_step()
             gs = rot.graphs(calls)
+            for g in {id(g): g for g in gs}.values():
+                g.replay()              # upload, untimed
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             for g in gs:
@@ -500,6 +537,8 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
             s = e0.elapsed_time(e1) / calls * 1e-3
             warm_rot = Rotation(torch, conv, rotate=False)
             gw = warm_rot.graphs(calls)
+            for g in {id(g): g for g in gw}.values():
+                g.replay()
             e0.record()
             for g in gw:
                 g.replay()
@@ -508,20 +547,22 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
             s_warm = e0.elapsed_time(e1) / calls * 1e-3
             iso = timed_calls(conv, 20, 2)
             key = "prepacked" if prepack else "oihw"
+            # fp32 on the tensor cores (three TF32 products) is held to that
+            # path's own compute ceiling; the CUDA-core FP32 peak stays as a
+            # second figure
+            split = L.dtype == "f32" and conv.algo == gb.ALGO_IGEMM_TC
+            t_c_run = L.flops() / (pc_split * 1e12) if split else t_c
             rec[key] = {
                 "algo": gb.algo_name(conv.algo),
                 "us_per_call": round(s * 1e6, 3),
                 "tflops": round(L.flops() / s / 1e12, 3),
                 "gbs": round(L.compulsory_bytes() / s / 1e9, 1),
-                "roofline_frac": round(t_ideal / s, 4),
-                "roofline_frac_at_3.35TBs": round(t_ideal_335 / s, 4),
-                "bound": ("tensor" if L.dtype != "f32" else "fp32") if t_c > t_m else "hbm",
-                # fp32 on the tensor cores (three TF32 products): the same
-                # time against that path's own compute ceiling
-                **({"roofline_frac_fp32_on_tensor_cores": round(
-                    max(L.flops() / (pc_split * 1e12), t_m) / s, 4)}
-                   if L.dtype == "f32" and conv.algo == gb.ALGO_IGEMM_TC else {}),
-                "compute_peak_tflops": round(pc, 1),
+                "roofline_frac": round(max(t_c_run, t_m) / s, 4),
+                "roofline_frac_at_3.35TBs": round(max(t_c_run, L.compulsory_bytes() / 3.35e12) / s, 4),
+                "bound": (("tensor" if split or L.dtype != "f32" else "fp32")
+                          if t_c_run > t_m else "hbm"),
+                **({"roofline_frac_vs_cuda_core_fp32_peak": round(t_ideal / s, 4)} if split else {}),
+                "compute_peak_tflops": round(pc_split if split else pc, 1),
                 "l2": rot.l2_note,
                 "us_per_call_l2_resident": round(s_warm * 1e6, 3),
                 "us_isolated_call_median": round(statistics.median(iso) * 1e3, 3),
@@ -628,7 +669,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(VARIANTS), default=DEFAULT_WORKLOAD)

@@ -4,12 +4,32 @@
 // githubissues.com/ysh329/OpenCL-101/52 ("init fault tolerance" and the
 // uninitialised-activation bug case): every field is checked, unknown enum
 // values are rejected, and nothing is launched for a rejected call.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 
 #include "internal.h"
 
 namespace gbconv {
+
+bool log_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("GBCONV_LOG");
+        return v && v[0] && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+void log_line(const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    std::fprintf(stderr, "gbconv: %s\n", buf);
+}
 
 namespace {
 
@@ -186,6 +206,13 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
         overlap(y, yb, d->workspace, ws.total) || overlap(d->workspace, ws.total, x, xb) ||
         overlap(d->workspace, ws.total, w, wb) || overlap(d->workspace, ws.total, b, bb))
         return GBCONV_ERR_OVERLAP;
+    if (log_enabled())
+        log_line("conv%dd N=%d C=%d D=%d H=%d W=%d OC=%d k=%d pad=%d stride=%d dtype=%d act=%d%s%s%s "
+                 "-> OD=%d OH=%d OW=%d algo=%s weights=%s workspace=%zu",
+                 ndim, p.N, p.C, p.D, p.H, p.W, p.OC, p.k, p.pad, p.stride, p.dtype, p.act,
+                 p.cl ? " channels_last" : "", p.pool ? " maxpool2" : "",
+                 p.pad_d != p.pad && ndim == 3 ? " frame_pad" : "", p.OD, p.YH, p.YW,
+                 gbconv_algo_name(p.algo), p.w_layout == GBCONV_W_PACKED ? "packed" : "oihw", ws.total);
     st = device_check();
     if (st != GBCONV_OK) return st;
 
@@ -226,12 +253,7 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
     default:
         return GBCONV_ERR_ALGO;
     }
-    if (e == cudaErrorInvalidValue) return GBCONV_ERR_CUDA;
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return GBCONV_ERR_LAUNCH;
-    }
-    return GBCONV_OK;
+    return launch_status(e);
 }
 
 }  // namespace

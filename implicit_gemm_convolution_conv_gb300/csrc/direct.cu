@@ -177,6 +177,9 @@ cudaError_t launch_tile(const Problem &p, const DirectArgs &a0, cudaStream_t st)
     if (e != cudaSuccess) return e;
     dim3 grid((p.OW + TW - 1) / TW, (p.OH + TH - 1) / TH,
               (unsigned)((int64_t)p.N * p.OD * a.oc_blocks));
+    if (log_enabled())
+        log_line("direct_conv_kernel grid=%ux%ux%u block=%d smem=%zu tile=%dx%d oc_block=%d", grid.x, grid.y,
+                 grid.z, TL::NT, smem, TH, TW, OCB);
     kern<<<grid, TL::NT, smem, st>>>(a);
     return cudaGetLastError();
 }

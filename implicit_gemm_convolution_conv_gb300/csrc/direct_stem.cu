@@ -381,6 +381,9 @@ cudaError_t launch_stem_csp(const Problem &p, const StemArgs &a0, cudaStream_t s
     a.warps_per_ocb = (int)per_ocb;
     const long long total_warps = per_ocb * a.oc_blocks;
     const int grid = (int)((total_warps + kWarps - 1) / kWarps);
+    if (log_enabled())
+        log_line("direct_stem_kernel grid=%d block=%d warps_per_oc_block=%d oc_blocks=%d pixel_tiles=%lld", grid,
+                 kWarps * 32, a.warps_per_ocb, a.oc_blocks, (long long)a.pix_tiles);
     kern<<<grid, kWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }

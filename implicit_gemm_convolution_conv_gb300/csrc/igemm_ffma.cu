@@ -310,10 +310,15 @@ cudaError_t launch_ffma_typed(const FfmaArgs &a, bool cl, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         dim3 grid((unsigned)((a.M + WBM - 1) / WBM), (a.OC + WBN - 1) / WBN);
+        if (log_enabled())
+            log_line("igemm_ffma2_kernel grid=%ux%u block=%d smem=%d tile=%dx%d", grid.x, grid.y, WNT, smem, WBM, WBN);
         kern<<<grid, WNT, smem, s>>>(a);
         return cudaGetLastError();
     }
     dim3 grid((unsigned)((a.M + BM - 1) / BM), (a.OC + BN - 1) / BN);
+    if (log_enabled())
+        log_line("igemm_ffma_kernel grid=%ux%u block=%d tile=%dx%d%s", grid.x, grid.y, NT, BM, BN,
+                 cl ? " channels_last" : "");
     igemm_ffma_kernel<T><<<grid, NT, 0, s>>>(a);
     return cudaGetLastError();
 }

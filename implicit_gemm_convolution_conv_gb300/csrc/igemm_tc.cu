@@ -281,14 +281,15 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     if (++s == a.stages) { s = 0; ph ^= 1u; }
                 }
             }
-            if (!ok) {
-                raise_abort(abort_flag);
-                // Let the copies already issued land before the CTA exits.
-                const int first = issued > a.stages ? issued - a.stages : 0;
-                for (int q = first; q < issued; ++q)
-                    wait_bounded(full0 + 8u * (q % a.stages), (uint32_t)(q / a.stages) & 1u, limit,
-                                 nullptr);
-            }
+            if (!ok) raise_abort(abort_flag);
+            // Let the copies already issued land before the CTA exits (on the
+            // normal path the MMA warp consumed them all; after an abort some
+            // may still be in flight). Copy q completes phase q / stages of
+            // its stage's barrier, the last phase issued on it.
+            const int first = issued > a.stages ? issued - a.stages : 0;
+            for (int q = first; q < issued; ++q)
+                wait_bounded(full0 + 8u * (q % a.stages), (uint32_t)(q / a.stages) & 1u, kDrainLimitCycles,
+                             nullptr);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -342,11 +343,12 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 }
                 if (ok) tc_commit(tfull0 + 8u * acc);
             }
-            if (!ok) {
-                raise_abort(abort_flag);
-                tc_commit(drain_bar);
-                wait_bounded(drain_bar, 0, limit, nullptr);
-            }
+            if (!ok) raise_abort(abort_flag);
+            // Every MMA this thread issued completes before TMEM is freed,
+            // also when the epilogue gave up before reading the last
+            // accumulator.
+            tc_commit(drain_bar);
+            wait_bounded(drain_bar, 0, kDrainLimitCycles, nullptr);
         }
         __syncwarp();
     } else {

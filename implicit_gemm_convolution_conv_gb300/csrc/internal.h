@@ -111,6 +111,24 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
+// Status of a forward call from the error its launches returned: a CUDA
+// call the library makes before launching (tensor-map encoding, attribute
+// set-up) reports cudaErrorInvalidValue and maps to GBCONV_ERR_CUDA; any
+// other launch error to GBCONV_ERR_LAUNCH (and is cleared).
+inline gbconv_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return GBCONV_OK;
+    if (e == cudaErrorInvalidValue) return GBCONV_ERR_CUDA;
+    cudaGetLastError();
+    return GBCONV_ERR_LAUNCH;
+}
+
+// Logging: with GBCONV_LOG=1 in the environment (read once per process)
+// every forward call writes its kernel choice, and each launcher its launch
+// geometry, as one line each to stderr. Host only; nothing is logged
+// otherwise.
+bool log_enabled();
+void log_line(const char *fmt, ...) __attribute__((format(printf, 1, 2)));
+
 // Device-side error word and wait limit (defined in igemm_tc.cu).
 uint64_t wait_limit_ns();
 void set_wait_limit_ns(uint64_t ns);

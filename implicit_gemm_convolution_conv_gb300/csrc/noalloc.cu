@@ -19,7 +19,12 @@
 //    at zero: each call rewrites every byte it reads, zero padding included.
 //  - The first call on a device looks up the array's device address with
 //    cudaGetSymbolAddress (with that device current) and caches it; make that
-//    first call before any stream capture begins.
+//    first call before any stream capture begins. The cached address belongs
+//    to the device's primary context: after cudaDeviceReset (or anything
+//    else that destroys that context) it is stale, so such a process must
+//    not call this entry point again.
+//  - The fused max pool (flags bit 2) lives only in the direct kernel, so a
+//    descriptor that asks for it is rejected with GBCONV_ERR_ALGO.
 #include <mutex>
 
 #include "internal.h"
@@ -108,9 +113,5 @@ extern "C" gbconv_status gbconv_conv_fwd_noalloc(const gbconv_desc *desc, int nd
     if (overlap(y, yb, scratch, wp_bytes)) return GBCONV_ERR_OVERLAP;
     cudaError_t e = launch_pack_ffma(p, w, scratch, stream);
     if (e == cudaSuccess) e = launch_igemm_ffma(p, x, scratch, b, y, stream);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return GBCONV_ERR_LAUNCH;
-    }
-    return GBCONV_OK;
+    return launch_status(e);   // the same mapping as the regular forward call
 }

@@ -177,14 +177,19 @@ __device__ __forceinline__ void stem_mmas(uint32_t tacc, uint32_t tA, uint32_t s
     }
 }
 
-// Bounded wait by lane 0 of each warp, result shared with the warp; an
-// expired wait sets the device error word.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long limit) {
+// Bounded wait by lane 0 of each warp, result shared with the warp. An
+// expired wait raises the CTA's abort flag and sets the device error word;
+// once the flag is up every later wait returns at once. The groups keep
+// their control flow after an abort (their named barriers stay matched) but
+// issue no further copy, MMA or store, so the drain at the end has at most
+// one commit and one copy per halo buffer to wait for.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long limit, volatile int *abort_flag) {
     int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, limit, nullptr);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok && (threadIdx.x & 31) == 0) atomicOr(&g_device_error, 1u);
-    return ok != 0;
+    if ((threadIdx.x & 31) == 0) {
+        ok = wait_bounded(bar, parity, limit, abort_flag);
+        if (!ok) raise_abort(abort_flag);
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // The pixel's T taps in (c, ky, kx) order from global memory, zero outside
@@ -290,6 +295,9 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const uint32_t slot_addr = sBar0 + 24u * (uint32_t)G;
     float *sBias = reinterpret_cast<float *>(smem_raw + (((slot_addr + 4u + 15u) & ~15u) - raw));   // 16-byte aligned
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem_raw + (slot_addr - raw));
+    // The abort flag sits in the 4 bytes after the TMEM address (sBias starts
+    // at least 8 bytes after it).
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem_raw + (slot_addr + 4u - raw));
 
     const int tid = threadIdx.x;
     const int g = tid / kStemPxThreads, gtid = tid % kStemPxThreads;   // group, pixel row in the tile
@@ -305,10 +313,15 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const bool active = tile < tend;
 
     pdl_launch_dependents();
-    // Per halo buffer, 1 + the barrier phase parity of a TMA load issued and
-    // not yet seen complete (0: none); kept by the group's thread 0.
+    // Kept by the group's thread 0: per halo buffer, 1 + the barrier phase
+    // parity of a TMA load issued and not yet seen complete (0: none); and
+    // the same for the group's last MMA commit. A copy or commit is issued
+    // only after the previous one on its barrier was seen complete, so the
+    // pending one is always its barrier's current phase.
     uint32_t halo_pending[2] = {0, 0};
+    uint32_t mma_pending = 0;
     float xv[T];
+    if (tid == 0) *abort_flag = 0;
     if (gtid == 0) {
         mbar_init(barM, 1);
         if (TMA) {
@@ -379,7 +392,6 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
 
     uint32_t mphase = 0;
-    bool any = false;
     if (TMA) {
         const int r = gtid / kStemTileW, j = gtid % kStemTileW;    // this thread's pixel in the tile
         const int s = a.stride;
@@ -387,8 +399,11 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         for (int k = 0; active; ++k) {
             const int hb = k & 1;
             const uint32_t hbuf = sHalo + (uint32_t)hb * a.halo_bytes;
-            const bool landed = warp_wait(barH + 8u * hb, (uint32_t)((k >> 1) & 1), a.wait_limit_cycles);
-            if (gtid == 0 && landed) halo_pending[hb] = 0;
+            const uint32_t hpar = (uint32_t)((k >> 1) & 1);
+            const bool landed = warp_wait(barH + 8u * hb, hpar, a.wait_limit_cycles, abort_flag);
+            // (after an abort no load follows, and a wait for the other
+            // parity may return at once without the pending load landing)
+            if (gtid == 0 && landed && halo_pending[hb] == 1u + hpar) halo_pending[hb] = 0;
             {
                 const float *h = reinterpret_cast<const float *>(smem_raw + (hbuf - raw));
                 if (pair_taps) {
@@ -426,7 +441,7 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             tc_fence_before();
             named_barrier(1 + g, kStemPxThreads);          // operand written, halo buffer hb read
             tc_fence_after();
-            if (gtid == 0) {
+            if (gtid == 0 && !*abort_flag) {
                 const int ahead = tile + 2 * tstep;
                 if (ahead < tend) {
                     stem_load_halo(&tmX, a, ahead, hbuf, barH + 8u * hb);
@@ -434,9 +449,10 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
                 }
                 stem_mmas<KP, ATM>(tacc, tA, sA, sB, bchunk, a.idesc);
                 tc_commit(barM);
+                mma_pending = 1u + mphase;
             }
-            any = true;
-            warp_wait(barM, mphase, a.wait_limit_cycles);
+            if (warp_wait(barM, mphase, a.wait_limit_cycles, abort_flag) && gtid == 0 && mma_pending == 1u + mphase)
+                mma_pending = 0;
             mphase ^= 1u;
             tc_fence_after();
             // Staging tile [oc][row][pixel].
@@ -465,7 +481,7 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             // TMEM reads complete before the group barrier that precedes the next MMAs.
             tc_fence_before();
             named_barrier(1 + g, kStemPxThreads);
-            if (gtid == 0) {
+            if (gtid == 0 && !*abort_flag) {
                 const StemTile st = stem_tile(a, tile);
                 const uint32_t box_bytes = (uint32_t)(a.ybox_c * kStemTileR * kStemTileW * 4);
                 for (int c0 = 0, bi = 0; c0 < a.OC; c0 += a.ybox_c, ++bi)
@@ -479,10 +495,10 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             // The stores must have read the staging tile before the CTA's
             // shared memory goes away; their global writes complete with the grid.
             bulk_wait_read_all();
-            // A halo wait that ran out leaves its load possibly in flight:
-            // wait for that buffer's barrier to complete a phase (bounded).
+            // After an abort a halo load may still be in flight: wait for it
+            // to land (it is the current phase of its buffer's barrier).
             for (int k = 0; k < 2; ++k)
-                if (halo_pending[k]) wait_bounded(barH + 8u * k, halo_pending[k] - 1u, a.wait_limit_cycles, nullptr);
+                if (halo_pending[k]) wait_bounded(barH + 8u * k, halo_pending[k] - 1u, kDrainLimitCycles, nullptr);
         }
     } else {
         while (active) {
@@ -490,18 +506,19 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             tc_fence_before();
             named_barrier(1 + g, kStemPxThreads);
             tc_fence_after();
-            if (gtid == 0) {
+            if (gtid == 0 && !*abort_flag) {
                 stem_mmas<KP, ATM>(tacc, tA, sA, sB, bchunk, a.idesc);
                 tc_commit(barM);
+                mma_pending = 1u + mphase;
             }
-            any = true;
             const int f = tile * kStemPxM + gtid;
             const bool valid = f < a.npix;
             const int n = valid ? f / a.ohw : 0;
             float *y_px = a.y + (long long)n * a.OC * a.ohw + (valid ? f - n * a.ohw : 0);
             const int next = tile + tstep;
             if (next < tend) stem_gather<C>(a, next * kStemPxM + gtid, xv);   // in flight during the wait
-            warp_wait(barM, mphase, a.wait_limit_cycles);
+            if (warp_wait(barM, mphase, a.wait_limit_cycles, abort_flag) && gtid == 0 && mma_pending == 1u + mphase)
+                mma_pending = 0;
             mphase ^= 1u;
             tc_fence_after();
             stem_epilogue(a, tacc + lane_off, sBias, y_px, valid);
@@ -510,9 +527,9 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
             tile = next;
         }
     }
-    // A wait that ran out leaves its MMAs possibly in flight: wait once more
-    // (bounded) for the group's last commit before the TMEM is released.
-    if (any && gtid == 0) wait_bounded(barM, mphase ^ 1u, a.wait_limit_cycles, nullptr);
+    // After an abort the group's last commit may still be in flight: its
+    // MMAs land before the TMEM is released.
+    if (gtid == 0 && mma_pending) wait_bounded(barM, mma_pending - 1u, kDrainLimitCycles, nullptr);
     tc_fence_before();
     __syncthreads();
     if (tid < 32) {
@@ -631,5 +648,8 @@ cudaError_t launch_stem_tf32_c(const Problem &p, const float *x, const float *w,
     // One CTA per SM (a kernel that uses TMEM is resident once per SM).
     const int ctas = (a.tiles + G - 1) / G;
     const int grid = ctas < info.sms ? ctas : info.sms;
+    if (log_enabled())
+        log_line("stem_tf32_kernel<C=%d> grid=%d block=%d smem=%zu groups=%d tiles=%d operand=%s io=%s", C, grid,
+                 kStemPxThreads * G, smem, G, a.tiles, atm ? "tmem" : "smem", tma ? "tma" : "plain");
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kStemPxThreads * G), smem, s, tmX, tmY, a);
 }

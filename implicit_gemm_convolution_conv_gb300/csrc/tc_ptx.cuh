@@ -39,19 +39,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Wait until the phase with the given parity has completed, for at most
-// `limit` SM cycles; gives up early when another role raised the abort flag.
+// `limit` SM cycles (checked after every unsuccessful try); gives up early
+// when another role raised the abort flag.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, long long limit,
                                              const volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    for (;;) {
 #pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (abort_flag && *abort_flag) return false;
+    for (int i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > limit) return false;
+        if ((i & 7) == 0 && abort_flag && *abort_flag) return false;
     }
 }
+// Bound of the waits that drain a CTA's own copies and MMAs before it exits
+// (about a second at the maximum SM clock). Work already issued always
+// completes, so this is only a backstop, independent of the limit the caller
+// set for the waits of normal operation: however short that limit, no CTA
+// leaves, or frees its TMEM, before its issued copies and MMAs have landed.
+constexpr long long kDrainLimitCycles = 1ll << 31;
 __device__ __forceinline__ void raise_abort(volatile int *flag) {
     *flag = 1;
     atomicOr(&g_device_error, 1u);

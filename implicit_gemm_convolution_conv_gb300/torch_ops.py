@@ -9,8 +9,9 @@ import copy
 import numpy as np
 import torch
 
-from . import (ACT_NONE, ACT_RELU, ALGO_AUTO, BF16, F16, F32, W_OIHW,
-               W_PACKED, GbconvError, check, conv2d_fwd, conv3d_fwd,
+from . import (ACT_NONE, ACT_RELU, ALGO_AUTO, BF16, F16, F32,
+               FLAG_CHANNELS_LAST, W_OIHW, W_PACKED, GbconvError, check,
+               conv2d_fwd, conv3d_fwd,
                make_desc, output_shape, select_algo, weight_pack,
                weight_packed_size, workspace_size)
 
@@ -83,9 +84,21 @@ def check_tensors(x, w, b=None, channels_last=False, require_cuda=True):
     return OC, k
 
 
-def output_tensor(x, OC, k, stride, pad):
-    sp = [(n + 2 * pad - k) // stride + 1 for n in x.shape[2:]]
-    return torch.empty([x.shape[0], OC] + sp, dtype=x.dtype, device=x.device)
+def y_shape(desc, ndim):
+    """y's shape for this desc, from gbconv_output_shape (frame padding,
+    fused pool and channels-last included), not from a formula restated
+    here."""
+    st, (od, oh, ow) = output_shape(desc, ndim)
+    check(st)
+    sp = [oh, ow] if ndim == 2 else [od, oh, ow]
+    if desc.flags & FLAG_CHANNELS_LAST:
+        return [desc.N] + sp + [desc.OC]
+    return [desc.N, desc.OC] + sp
+
+
+def output_tensor(desc, ndim, x):
+    """An uninitialised y for this desc, with x's dtype, on x's device."""
+    return torch.empty(y_shape(desc, ndim), dtype=x.dtype, device=x.device)
 
 
 class Conv:
@@ -128,10 +141,7 @@ class Conv:
             # the tensor's real size: the library refuses one that is too small
             self.desc.workspace_bytes = workspace.numel() * workspace.element_size()
         self.workspace = workspace
-        st, (od, oh, ow) = output_shape(self.desc, self.nsp)
-        check(st)
-        sp = [oh, ow] if self.nsp == 2 else [od, oh, ow]
-        shape = [x.shape[0]] + sp + [OC] if channels_last else [x.shape[0], OC] + sp
+        shape = y_shape(self.desc, self.nsp)
         if out is None:
             out = torch.empty(shape, dtype=x.dtype, device=x.device)
         elif (list(out.shape) != shape or out.dtype != x.dtype or out.device != x.device or

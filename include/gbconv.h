@@ -284,14 +284,18 @@ gbconv_status gbconv_set_wait_limit_ns(uint64_t ns);
  *   desc      as for gbconv_conv2d_fwd; algo must be AUTO or IGEMM_FFMA,
  *             w_layout must be OIHW, workspace fields are ignored.
  *   x, w, b, y  caller-owned device pointers, as for gbconv_conv2d_fwd.
- * Errors: the usual validation codes; GBCONV_ERR_TOO_LARGE when the packed
- * weights (taps * C * roundup(OC, 128) elements of the storage type) exceed
- * the fixed array.
+ * Errors: the validation codes of gbconv_conv2d_fwd, except that the fused
+ * 2x2 max pool (flags bit 2), which only the direct kernel has, is always
+ * GBCONV_ERR_ALGO here; GBCONV_ERR_TOO_LARGE when the packed weights
+ * (taps * C * roundup(OC, 128) elements of the storage type) exceed the
+ * fixed array; GBCONV_ERR_CUDA / GBCONV_ERR_LAUNCH as for the forward call.
  * All calls on a device share the array: calls whose kernels overlap on the
  * GPU race, so serialise them on one stream. The array keeps the last call's
  * contents; every call rewrites all of it that it reads. The first call on a
  * device looks up the array's address (cudaGetSymbolAddress, that device
- * current); make that first call before any stream capture.
+ * current); make that first call before any stream capture. That address is
+ * cached for the life of the device's primary context: after cudaDeviceReset
+ * the process must not call this entry point again.
  */
 #define GBCONV_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 gbconv_status gbconv_conv_fwd_noalloc(const gbconv_desc *desc, int ndim,

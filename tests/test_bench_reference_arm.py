@@ -28,8 +28,22 @@ def _line(stdout):
     return json.loads(lines[0])
 
 
-def test_reference_arm_prints_one_contract_line():
+def test_reference_arm_default_workload_is_the_video_vae_conv3d():
     r = _run(["--impl", "reference", "--steps", "3", "--warmup", "3"])
+    assert r.returncode == 0, r.stderr
+    d = _line(r.stdout)
+    assert d["impl"] == "reference"
+    assert d["config"]["workload"] == "conv3d_f16_1x128x5x128x240_oc128_k3p1s1"
+    # a step is a seeded sample of n outputs: value = n/total of the
+    # layer's FLOP per step time
+    n, total = [int(v) for v in d["cpu_baseline"]["sample"].split(" outputs")[0].split(" of ")]
+    flop = 2 * 128 * 5 * 128 * 240 * 128 * 27 * n / total
+    assert abs(d["value"] - flop / (d["ms_per_step"] * 1e-3) / 1e12) <= 0.02 * d["value"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _run(["--impl", "reference", "--steps", "3", "--warmup", "3",
+              "--workload", "detection_stem"])
     assert r.returncode == 0, r.stderr
     d = _line(r.stdout)
     assert d["impl"] == "reference"

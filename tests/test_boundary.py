@@ -360,3 +360,29 @@ def test_make_desc_refuses_values_wider_than_a_c_int():
         args.update(kw)
         with pytest.raises(ValueError):
             gb.make_desc(**args)
+
+
+@pytest.mark.skipif(HAVE_GPU, reason="checks the host-side log line on a machine without a GPU")
+def test_gbconv_log_writes_the_kernel_choice_to_stderr():
+    """GBCONV_LOG=1: a forward call writes one line with its shape, frame
+    padding, algorithm, weight layout and workspace to stderr (here the call
+    then stops at the device check, as there is no GPU). Without the
+    variable nothing is written."""
+    import sys
+    code = (
+        "import implicit_gemm_convolution_conv_gb300 as gb\n"
+        "d = gb.make_desc(1, 128, 128, 240, 128, 3, 1, 1, D=5, dtype=gb.F16, tpad=gb.TPAD_CAUSAL,\n"
+        "                 workspace=1 << 32, workspace_bytes=1 << 30)\n"
+        "print(gb.conv3d_fwd(d, 1 << 20, 1 << 28, None, 1 << 29, 0))\n")
+    env = dict(os.environ, GBCONV_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert int(r.stdout.strip()) == gb.ERR_UNSUPPORTED_DEVICE
+    line = [l for l in r.stderr.splitlines() if l.startswith("gbconv: conv3d")]
+    assert len(line) == 1, r.stderr
+    assert "algo=igemm_tc" in line[0] and "frame_pad" in line[0] and "OD=5 OH=128 OW=240" in line[0]
+    env.pop("GBCONV_LOG")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "gbconv:" not in r.stderr
