@@ -2,14 +2,18 @@
 //
 // GEMM view of the convolution sum (lpnh.cn/news/2745477 section 2.2; the
 // Convolution3D extension of git.erdda.com/Tencent/ncnn/discussions/7001
-// section 3.2): M = 128 output channels, N = up to 256 output pixels of one
-// (n, od) plane tile, K = taps x input channels. The A operand is the weight
-// slab of one tap, packed once as [tap][OC][C] (the page's "re-arrange
-// weights at export time", sections 2.3 and 4.2). The B operand is the input
-// shifted by that tap, which TMA fetches straight from a channels-last copy
-// of x as a {64 ch, BW px, BH rows, 1 frame, 1 image} box: padding is TMA's
-// out-of-bounds zero fill and the stride is TMA's element stride, so no
-// im2col buffer exists.
+// section 3.2): M = 128 output channels, N = NP consecutive output pixels in
+// (n, od, oh, ow) order (a tile may cross rows, frames and images), K = taps
+// x input channels. The A operand is the weight slab of one tap, packed once
+// as [tap][OC][C] (the page's "re-arrange weights at export time", sections
+// 2.3 and 4.2). The B operand is the input shifted by that tap, which TMA
+// fetches straight from a channels-last copy of x in im2col mode: one load
+// brings NP pixel rows of one 128-byte channel block, each pixel read at its
+// stride-spaced position plus the tap offset, with positions outside the
+// input read as zero (the padding). No im2col buffer exists. Because a tile
+// is any run of NP pixels, NP is chosen so that the tiles spread evenly over
+// the SMs (for example 148 tiles of 224 pixels for a 128 x 128 x 256-channel
+// layer, where whole-row tiles gave 128 tiles for 152 SMs).
 //
 // Persistent kernel, one CTA per SM, tiles handed out round-robin. Roles
 // (320 threads): warp 0 lane 0 issues TMA loads into a STAGES-deep
@@ -103,45 +107,51 @@ struct TcArgs {
     void *y;
     int OC, OD, OH, OW;
     int k, pad, pad_d, stride;
-    int BW, BH, NP;        // pixel tile: BH rows x BW columns; NP = MMA N >= BW*BH
-    int tiles_w, tiles_h, oc_tiles;
+    long long out_vol;     // OD * OH * OW: pixels of one image's output
+    long long P;           // N * out_vol: output pixels, in (n, od, oh, ow) order
+    int NP;                // pixels per tile = MMA N (a multiple of 32)
+    int oc_tiles;
     int num_tiles;
     int cblocks;
     int cs;                // fp32 split: channels of the hi half (the lo half starts there)
-    int x_paired;          // fp32 split: x_hi and x_lo come in one box (conv2d)
-    uint32_t xlo_off;      // fp32 split: byte offset of the x_lo tile in a stage (BW * BH * 128)
+    uint32_t xlo_off;      // fp32 split: byte offset of the x_lo rows in a stage (NP * 128)
     int ksteps;
     int stages;
     int relu;
-    int vec_store;         // 16-byte stores of 8 pixels (aligned rows and tiles)
+    int vec_store;         // NC(D)HW register stores as 16-byte vectors (out_vol % 8 == 0, y aligned)
     int cl;                // channels-last output [N][OD][OH][OW][OC]
     int pair_store;        // channels-last: 4-byte stores of channel pairs (OC even, y 4-byte aligned)
     int tma_store;         // staged chunks leave as TMA tensor stores (tmY valid)
     int single_tile;       // every CTA owns at most one tile: the staging tiles reuse the stage ring
     int prefetch;          // L2 prefetch before the dependency wait: 1 x (read in place), 2 packed weights too
-    int in_w, in_h, in_d;  // input extents (prefetch boxes start inside them)
+    int in_w, in_h, in_d;  // input extents (prefetch starts are clamped into them)
     uint32_t idesc;
     uint32_t tx_bytes;
     uint32_t tmem_cols;
     long long wait_limit_cycles;
 };
 
+// A tile: NP consecutive output pixels from linear pixel p0 (any row, frame
+// or image boundary inside it), times 128 output channels from oc0.
 struct TileCoord {
-    int n, od, oh0, ow0, oc0;
+    long long p0;
+    int n, od, oh, ow, oc0;
 };
 // Tile t: output-channel block fastest (consecutive CTAs share the pixels,
-// the weights of a block are read by every CTA), then the pixel tiles.
+// the weights of a block are read by every CTA), then the pixel runs.
 __device__ __forceinline__ TileCoord tile_coord(const TcArgs &a, int t) {
     TileCoord c;
     const int ot = t % a.oc_tiles;
-    t /= a.oc_tiles;
-    const int tw = t % a.tiles_w; t /= a.tiles_w;
-    const int th = t % a.tiles_h; t /= a.tiles_h;
-    c.od = t % a.OD;
-    c.n = t / a.OD;
-    c.ow0 = tw * a.BW;
-    c.oh0 = th * a.BH;
+    c.p0 = (long long)(t / a.oc_tiles) * a.NP;
     c.oc0 = ot * kTileOc;
+    const long long n = c.p0 / a.out_vol;
+    long long r = c.p0 - n * a.out_vol;
+    const long long plane = (long long)a.OH * a.OW;
+    c.n = (int)n;
+    c.od = (int)(r / plane);
+    r -= (long long)c.od * plane;
+    c.oh = (int)(r / a.OW);
+    c.ow = (int)(r - (long long)c.oh * a.OW);
     return c;
 }
 
@@ -156,7 +166,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     // A stage: weights (one 16 KB tile, or [w_hi | w_lo] for fp32), then the
-    // pixels (NP rows of 128 B, or [x_hi | x_lo] for fp32).
+    // pixels (NP rows of 128 B, or x_hi rows then x_lo rows for fp32).
     constexpr uint32_t w_stage = TcElt<T>::kSplit ? 2u * kWStageBytes : kWStageBytes;
     const uint32_t x_stage = (TcElt<T>::kSplit ? 2u : 1u) * (uint32_t)a.NP * 128u;
     const uint32_t sW = base;
@@ -197,20 +207,19 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         // The first ring's worth of the first tile's boxes, for operands that
         // no kernel of this call writes, start towards L2 while the previous
         // kernel finishes (L2 is where the GPU's writes become coherent, so
-        // the loads after the wait cannot see stale data). Starts are
-        // clamped to the tensor: a hint needs no zero fill.
+        // the loads after the wait cannot see stale data). The pixel run's
+        // start is clamped into the tensor: a hint needs no zero fill.
         if (!TcElt<T>::kSplit && a.prefetch && (int)blockIdx.x < a.num_tiles) {
             const TileCoord tc = tile_coord(a, blockIdx.x);
-            const int x0 = tc.ow0 * a.stride - a.pad, y0 = tc.oh0 * a.stride - a.pad,
-                      z0 = tc.od * a.stride - a.pad_d;
-            int cb = 0, tap = 0, kx = 0, ky = 0, kz = 0;
+            const int x0 = max(tc.ow * a.stride - a.pad, 0), y0 = max(tc.oh * a.stride - a.pad, 0),
+                      z0 = max(tc.od * a.stride - a.pad_d, 0);
+            int cb = 0, kx = 0, ky = 0, kz = 0, tap = 0;
             for (int it = 0; it < a.stages && it < a.ksteps; ++it) {
                 const int c0 = cb * TcElt<T>::kBlk;
                 if (a.prefetch & 2) tma_prefetch_l2_3d(&tmW, c0, tc.oc0, tap);
-                const int xs = x0 + kx > 0 ? x0 + kx : 0, ys = y0 + ky > 0 ? y0 + ky : 0,
-                          zs = z0 + kz > 0 ? z0 + kz : 0;
-                if ((a.prefetch & 1) && xs < a.in_w && ys < a.in_h && zs < a.in_d)
-                    tma_prefetch_l2_5d(&tmX, c0, xs, ys, zs, tc.n);
+                if ((a.prefetch & 1) && x0 + kx < a.in_w && y0 + ky < a.in_h && z0 + kz < a.in_d)
+                    tma_prefetch_l2_im2col_5d(&tmX, c0, x0, y0, z0, tc.n, (uint16_t)kx, (uint16_t)ky,
+                                              (uint16_t)kz);
                 if (++cb == a.cblocks) {
                     cb = 0;
                     ++tap;
@@ -245,7 +254,8 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             bool ok = true;
             for (int t = blockIdx.x; t < a.num_tiles && ok; t += gridDim.x) {
                 const TileCoord tc = tile_coord(a, t);
-                const int x0 = tc.ow0 * a.stride - a.pad, y0 = tc.oh0 * a.stride - a.pad,
+                // traversal position of the tile's first pixel
+                const int x0 = tc.ow * a.stride - a.pad, y0 = tc.oh * a.stride - a.pad,
                           z0 = tc.od * a.stride - a.pad_d;
                 int cb = 0, tap = 0, kx = 0, ky = 0, kz = 0;
                 for (int it = 0; it < a.ksteps; ++it) {
@@ -259,15 +269,14 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     mbar_arrive_expect_tx(fb, a.tx_bytes);
                     if constexpr (TcElt<T>::kSplit) {
                         tma_load_4d(dw, &tmW, fb, c0, tc.oc0, 0, tap);              // [w_hi | w_lo]
-                        if (a.x_paired) {
-                            tma_load_5d(dx, &tmX, fb, c0, x0 + kx, y0 + ky, 0, tc.n);   // [x_hi | x_lo]
-                        } else {
-                            tma_load_5d(dx, &tmX, fb, c0, x0 + kx, y0 + ky, z0 + kz, tc.n);
-                            tma_load_5d(dx + a.xlo_off, &tmX, fb, a.cs + c0, x0 + kx, y0 + ky, z0 + kz, tc.n);
-                        }
+                        tma_load_im2col_5d(dx, &tmX, fb, c0, x0, y0, z0, tc.n, (uint16_t)kx, (uint16_t)ky,
+                                           (uint16_t)kz);                            // x_hi
+                        tma_load_im2col_5d(dx + a.xlo_off, &tmX, fb, a.cs + c0, x0, y0, z0, tc.n, (uint16_t)kx,
+                                           (uint16_t)ky, (uint16_t)kz);              // x_lo
                     } else {
                         tma_load_3d(dw, &tmW, fb, c0, tc.oc0, tap);
-                        tma_load_5d(dx, &tmX, fb, c0, x0 + kx, y0 + ky, z0 + kz, tc.n);
+                        tma_load_im2col_5d(dx, &tmX, fb, c0, x0, y0, z0, tc.n, (uint16_t)kx, (uint16_t)ky,
+                                           (uint16_t)kz);
                     }
                     ++issued;
                     if (++cb == a.cblocks) {
@@ -357,9 +366,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         // warps of a quadrant take alternate 32-pixel column chunks.
         const int q = warp & 3;
         const int grp = (warp - 2) / 4;
-        const int MT = a.BW * a.BH;
-        const int nchunks = (MT + kColChunk - 1) / kColChunk;
-        const int64_t plane = (int64_t)a.OH * a.OW;
+        const int nchunks = a.NP / kColChunk;
         const uint32_t ystage = sY + (uint32_t)(warp - 2) * 2u * TcElt<T>::kChunkBytes;
         int nst = 0;             // TMA stores this warp has issued
         int local = 0;
@@ -380,27 +387,20 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             const float bias = (a.b && oc_ok) ? __ldg(a.b + oc) : 0.0f;
             const bool odd = lane & 1;
             const int oc_even = oc - (odd ? 1 : 0);
-            // Channels-last: pixel (r, c) of the tile is at ((n OD + od) OH +
-            // oh0 + r) OW + ow0 + c, its channel oc at that times OC + oc.
-            // NCHW: channel oc's plane, pixel at (oh0 + r) OW + ow0 + c.
-            T *const ybase = a.cl ? static_cast<T *>(a.y) + ((int64_t)tc.n * a.OD + tc.od) * plane * a.OC
-                                  : static_cast<T *>(a.y) +
-                                        ((int64_t)tc.n * a.OC + (oc_ok ? oc : 0)) * a.OD * plane +
-                                        (int64_t)tc.od * plane;
-            // One 32-pixel chunk: its first pixel is row r0, column c0 of the
-            // tile. A chunk that lies in one row and inside the output takes
-            // the unchecked path; others step (r, c) pixel by pixel.
+            // One 32-pixel chunk, pixels pc .. pc + 31 of the (n, od, oh, ow)
+            // order (those past P do not exist). NC(D)HW: pixel pc is element
+            // v0 of image n0's plane of each channel; channels-last: row pc
+            // of the [P][OC] matrix.
             auto store_chunk = [&](const uint32_t (&v)[32], int ch) {
-                const int p0 = ch * kColChunk;
-                const int r0 = p0 / a.BW, c0 = p0 - r0 * a.BW;
-                const bool whole = c0 + kColChunk <= a.BW && r0 < a.BH && tc.oh0 + r0 < a.OH &&
-                                   tc.ow0 + c0 + kColChunk <= a.OW;
-                const int64_t pix0 = (int64_t)(tc.oh0 + r0) * a.OW + tc.ow0 + c0;
-                // One box: the chunk lies in row r0 of the tile, or runs past
-                // the tile's last row only where the image edge clips it.
-                if (a.tma_store && r0 < a.BH &&
-                    (c0 + kColChunk <= a.BW || (r0 == a.BH - 1 && tc.ow0 + a.BW >= a.OW))) {
-                    if (tc.oh0 + r0 >= a.OH) return;
+                const long long pc = tc.p0 + (long long)ch * kColChunk;
+                if (pc >= a.P) return;
+                const int nv = a.P - pc < kColChunk ? (int)(a.P - pc) : kColChunk;
+                const long long n0 = pc / a.out_vol;
+                const long long v0 = pc - n0 * a.out_vol;
+                const bool one_image = v0 + kColChunk <= a.out_vol || n0 + 1 == a.P / a.out_vol;
+                // One box: a channels-last chunk always; an NC(D)HW chunk that
+                // lies in one image's planes (the tensor's end clips the last).
+                if (a.tma_store && (a.cl || one_image)) {
                     const uint32_t buf = ystage + (uint32_t)(nst & 1) * TcElt<T>::kChunkBytes;
                     if (nst >= 2) {
                         // The store that last used this buffer has read it.
@@ -441,10 +441,10 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         const uint32_t cb = (uint32_t)(lane & ~1) * 2u;      // byte of channel pair
 #pragma unroll
                         for (int e = 0; e < kColChunk; e += 2) {
-                            const float v0 = epilogue(__uint_as_float(v[e]), bias, a.relu);
-                            const float v1 = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
-                            const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-                            const typename Storage<T>::Pair pr = Storage<T>::pack2(odd ? got : v0, odd ? v1 : got);
+                            const float v0f = epilogue(__uint_as_float(v[e]), bias, a.relu);
+                            const float v1f = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
+                            const float got = __shfl_xor_sync(0xffffffffu, odd ? v0f : v1f, 1);
+                            const typename Storage<T>::Pair pr = Storage<T>::pack2(odd ? got : v0f, odd ? v1f : got);
                             const int row = e + (odd ? 1 : 0);
                             const uint32_t addr = buf + (uint32_t)row * 64u +
                                                   ((((cb >> 4) ^ (uint32_t)((row >> 1) & 3)) << 4) | (cb & 15u));
@@ -452,7 +452,7 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                                          "r"(*reinterpret_cast<const uint32_t *>(&pr))
                                          : "memory");
                         }
-                    } else {
+                      } else {
                         // [channel][pixel] rows of 64 B: this lane's channel, 32 pixels.
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -475,56 +475,45 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     if (lane == 0) {
                         const int chan = tc.oc0 + q * 32;
                         if (a.cl)
-                            tma_store_5d(&tmY, buf, chan, tc.ow0 + c0, tc.oh0 + r0, tc.od, tc.n);
+                            tma_store_2d(&tmY, buf, chan, (int)pc);
                         else
-                            tma_store_5d(&tmY, buf, tc.ow0 + c0, tc.oh0 + r0, tc.od, chan, tc.n);
+                            tma_store_3d(&tmY, buf, (int)v0, chan, (int)n0);
                         bulk_commit_group();
                     }
                     ++nst;
                     return;
                 }
                 if (a.cl) {
+                    T *const yrow = static_cast<T *>(a.y) + pc * a.OC;     // pixel pc, channel 0
                     if (!TcElt<T>::kSplit && a.pair_store) {
                         // Even lanes keep pixel e, odd lanes pixel e + 1; each
                         // lane gets its partner's value of that pixel and
                         // stores the channel pair (oc_even, oc_even + 1).
                         const bool oc_pair_ok = oc_even < a.OC;
-                        int r = r0, c = c0 + (odd ? 1 : 0);
-                        if (c >= a.BW) { c -= a.BW; ++r; }
-                        T *yp = ybase + (pix0 + (odd ? 1 : 0)) * a.OC + oc_even;
 #pragma unroll
                         for (int e = 0; e < kColChunk; e += 2) {
-                            const float v0 = epilogue(__uint_as_float(v[e]), bias, a.relu);
-                            const float v1 = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
-                            const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                            const float v0f = epilogue(__uint_as_float(v[e]), bias, a.relu);
+                            const float v1f = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
+                            const float got = __shfl_xor_sync(0xffffffffu, odd ? v0f : v1f, 1);
                             const typename Storage<T>::Pair pr =
-                                Storage<T>::pack2(odd ? got : v0, odd ? v1 : got);
-                            if (whole) {
-                                if (oc_pair_ok)
-                                    *reinterpret_cast<typename Storage<T>::Pair *>(yp + (int64_t)e * a.OC) = pr;
-                            } else {
-                                if (oc_pair_ok && r < a.BH && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
-                                    *reinterpret_cast<typename Storage<T>::Pair *>(
-                                        ybase + ((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc_even) = pr;
-                                c += 2;
-                                if (c >= a.BW) { c -= a.BW; ++r; }
-                            }
+                                Storage<T>::pack2(odd ? got : v0f, odd ? v1f : got);
+                            const int px = e + (odd ? 1 : 0);
+                            if (oc_pair_ok && px < nv)
+                                *reinterpret_cast<typename Storage<T>::Pair *>(yrow + (long long)px * a.OC + oc_even) = pr;
                         }
                     } else if (oc_ok) {
-                        int r = r0, c = c0;
 #pragma unroll
-                        for (int e = 0; e < kColChunk; ++e) {
-                            if (r < a.BH && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
-                                ybase[((int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c) * a.OC + oc] =
+                        for (int e = 0; e < kColChunk; ++e)
+                            if (e < nv)
+                                yrow[(long long)e * a.OC + oc] =
                                     Storage<T>::from_float(epilogue(__uint_as_float(v[e]), bias, a.relu));
-                            if (++c == a.BW) { c = 0; ++r; }
-                        }
                     }
                     return;
                 }
                 if (!oc_ok) return;
-                if (!TcElt<T>::kSplit && a.vec_store && whole) {
-                    // 16-byte vectors of 8 consecutive pixels (rows and tiles 8-aligned).
+                if (!TcElt<T>::kSplit && a.vec_store && nv == kColChunk && v0 + kColChunk <= a.out_vol) {
+                    // 16-byte vectors of 8 consecutive pixels of one plane.
+                    T *dst = static_cast<T *>(a.y) + ((long long)n0 * a.OC + oc) * a.out_vol + v0;
 #pragma unroll
                     for (int i8 = 0; i8 < kColChunk / 8; ++i8) {
                         typename Storage<T>::Pair h[4];
@@ -532,16 +521,17 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                         for (int e = 0; e < 4; ++e)
                             h[e] = Storage<T>::pack2(epilogue(__uint_as_float(v[8 * i8 + 2 * e]), bias, a.relu),
                                                      epilogue(__uint_as_float(v[8 * i8 + 2 * e + 1]), bias, a.relu));
-                        *reinterpret_cast<uint4 *>(ybase + pix0 + 8 * i8) = *reinterpret_cast<const uint4 *>(h);
+                        *reinterpret_cast<uint4 *>(dst + 8 * i8) = *reinterpret_cast<const uint4 *>(h);
                     }
                 } else {
-                    int r = r0, c = c0;
+                    // pixel by pixel, moving to the next image's plane at its end
+                    long long n = n0, vv = v0;
 #pragma unroll
                     for (int e = 0; e < kColChunk; ++e) {
-                        if (r < a.BH && tc.oh0 + r < a.OH && tc.ow0 + c < a.OW)
-                            ybase[(int64_t)(tc.oh0 + r) * a.OW + tc.ow0 + c] =
+                        if (e < nv)
+                            static_cast<T *>(a.y)[(n * a.OC + oc) * a.out_vol + vv] =
                                 Storage<T>::from_float(epilogue(__uint_as_float(v[e]), bias, a.relu));
-                        if (++c == a.BW) { c = 0; ++r; }
+                        if (++vv == a.out_vol) { vv = 0; ++n; }
                     }
                 }
             };
@@ -718,6 +708,22 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
+PFN_cuTensorMapEncodeIm2col_v12000 get_encode_im2col() {
+    static PFN_cuTensorMapEncodeIm2col_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
 // SM count and clock of the current device, looked up once per device.
 struct DevInfo {
     int sms = 0;
@@ -742,86 +748,65 @@ cudaError_t dev_info(DevInfo *out) {
     return cudaSuccess;
 }
 
-// Pixel-tile geometry: BH rows x BW columns of one (n, od) plane, at most 256
-// pixels (MMA N, rounded up to a multiple of 16), boxes of at most 256
-// traversed elements per axis; whole output rows when they fit.
+// Tile geometry: NP consecutive output pixels (a multiple of 32, at most
+// 256: the MMA's N) per tile, and the depth of the stage ring.
 struct TileGeom {
-    int BW, BH, NP, stages;
+    int NP, stages;
+    bool single_tile;      // tiles <= SMs: the epilogue stages its outputs in the idle ring
 };
 
 uint32_t ystage_bytes(const Problem &p) {
     return p.dtype == GBCONV_F32 ? TcElt<float>::kStageBytes : TcElt<__half>::kStageBytes;
 }
 
-// Rows per tile when whole rows fit: the count whose tiles cost least on
-// `sms` SMs, a tile's MMA time taken as max(48, NP / 2) cycles per
-// instruction (the measured f16 rates: 45.5 / 48 / 64 / 128 cycles at N =
-// 32 / 64 / 128 / 256); ties go to taller tiles (fewer prologues).
-int rows_per_tile(const Problem &p, int bh_cap, int sms) {
-    int best = 1;
-    int64_t best_cost = -1;
-    const int oc_tiles = (p.OC + kTileOc - 1) / kTileOc;
-    for (int bh = bh_cap; bh >= 1; --bh) {
-        const int np = (p.OW * bh + 15) / 16 * 16;
-        const int64_t tiles = (int64_t)p.N * p.OD * ((p.OH + bh - 1) / bh) * oc_tiles;
-        const int64_t waves = (tiles + sms - 1) / sms;
-        const int64_t cost = waves * (np / 2 > 48 ? np / 2 : 48);
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = bh;
-        }
-    }
-    return best;
-}
+int64_t out_pixels(const Problem &p) { return (int64_t)p.N * p.out_vol; }
 
-TileGeom choose_geom(const Problem &p, int sms, bool *single_tile = nullptr) {
-    TileGeom g{};
-    const int bw_max = 256 / p.stride;
-    if (p.OW > bw_max) {
-        const int tiles = (p.OW + bw_max - 1) / bw_max;
-        g.BW = (p.OW + tiles - 1) / tiles;
-        const int bw8 = (g.BW + 7) / 8 * 8;          // 16-byte aligned column tiles
-        if (bw8 <= bw_max && (p.OW + bw8 - 1) / bw8 == tiles) g.BW = bw8;
-        g.BH = 1;
-    } else {
-        g.BW = p.OW;
-        int bh = 256 / p.OW;
-        const int bh_max = 256 / p.stride;
-        if (bh > bh_max) bh = bh_max;
-        if (bh > p.OH) bh = p.OH;
-        g.BH = rows_per_tile(p, bh < 1 ? 1 : bh, sms);
-        // fp32 stages hold two halves: keep the tile short enough for two of
-        // them next to the epilogue's staging.
-        while (p.dtype == GBCONV_F32 && g.BH > 1 &&
-               (227 * 1024 - 1024 - (int)ystage_bytes(p) - 256) /
-                       (2 * ((int)kWStageBytes + (g.BW * g.BH + 15) / 16 * 16 * 128)) < 2)
-            --g.BH;
-    }
-    g.NP = (g.BW * g.BH + 15) / 16 * 16;
-    // One tile per CTA: the epilogue stages its outputs in the idle ring.
-    const int64_t tiles = (int64_t)p.N * p.OD * ((p.OH + g.BH - 1) / g.BH) * ((p.OW + g.BW - 1) / g.BW) *
-                          ((p.OC + kTileOc - 1) / kTileOc);
-    const bool single = tiles <= sms;
+// Ring depth for NP pixels per tile (0 when two stages do not fit).
+int stages_for(const Problem &p, int np, bool single) {
     const int split = p.dtype == GBCONV_F32 ? 2 : 1;
-    const int stage_bytes = split * ((int)kWStageBytes + g.NP * 128);
+    const int stage_bytes = split * ((int)kWStageBytes + np * 128);
     const int fixed = 1024 + (single ? 0 : (int)ystage_bytes(p)) + 256;
     int st = (227 * 1024 - fixed) / stage_bytes;
-    g.stages = st > kMaxStages ? kMaxStages : st;
-    if (single && (int64_t)g.stages * stage_bytes < (int64_t)ystage_bytes(p)) {
-        // (never for the tile sizes here: the ring is at least 2 x 18 KB)
-        st = (227 * 1024 - 1024 - (int)ystage_bytes(p) - 256) / stage_bytes;
-        g.stages = st > kMaxStages ? kMaxStages : st;
-        if (single_tile) *single_tile = false;
-    } else if (single_tile) {
-        *single_tile = single;
+    if (st > kMaxStages) st = kMaxStages;
+    // the epilogue's staging reuses the ring of a single-tile CTA
+    if (single && (int64_t)st * stage_bytes < (int64_t)ystage_bytes(p)) return 0;
+    return st >= 2 ? st : 0;
+}
+
+// Pixels per tile: tiles are runs of consecutive output pixels (TMA im2col
+// loads cross rows, frames and images), so any multiple of 32 up to 256
+// works. The choice minimises waves x (one MMA's cycles), with the measured
+// f16 MMA time at M = 128 taken as max(N / 2, 32 + N / 4) cycles (full rate
+// from N = 128; below that the shared-memory operand reads set it); ties go
+// to larger tiles. Every MMA of a K step has this N, so the K loop length
+// cancels out.
+TileGeom choose_geom(const Problem &p, int sms) {
+    TileGeom g{};
+    const int64_t P = out_pixels(p);
+    const int64_t oc_tiles = (p.OC + kTileOc - 1) / kTileOc;
+    int64_t best_cost = -1;
+    for (int np = 256; np >= 32; np -= 32) {
+        const int64_t tiles = (P + np - 1) / np * oc_tiles;
+        const bool single = tiles <= sms;
+        const int st = stages_for(p, np, single);
+        if (st == 0) continue;
+        const int64_t waves = (tiles + sms - 1) / sms;
+        const int64_t mma = np / 2 > 32 + np / 4 ? np / 2 : 32 + np / 4;
+        const int64_t cost = waves * mma;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            g.NP = np;
+            g.stages = st;
+            g.single_tile = single;
+        }
     }
     return g;
 }
 
-size_t smem_bytes(const TileGeom &g, const Problem &p, bool single_tile) {
+size_t smem_bytes(const TileGeom &g, const Problem &p) {
     const size_t split = p.dtype == GBCONV_F32 ? 2 : 1;
     return 1024 + (size_t)g.stages * split * (kWStageBytes + (size_t)g.NP * 128) +
-           (single_tile ? 0 : ystage_bytes(p)) + 256;
+           (g.single_tile ? 0 : ystage_bytes(p)) + 256;
 }
 
 uint32_t tmem_cols_for(int cols) {
@@ -830,16 +815,36 @@ uint32_t tmem_cols_for(int cols) {
     return c;
 }
 
+// Pixel-box corners of the im2col traversal along W, H and D: positions run
+// from -pad (front) to extent - 1 + pad_back - (k - 1), i.e. one per output
+// coordinate at the conv stride. The 5-D form holds corners in [-16, 15].
+struct Corners {
+    int lo[3], hi[3];
+    bool ok;
+};
+Corners im2col_corners(const Problem &p) {
+    Corners c{};
+    c.lo[0] = c.lo[1] = -p.pad;
+    c.hi[0] = c.hi[1] = p.pad - (p.k - 1);
+    c.lo[2] = -p.pad_d;
+    c.hi[2] = p.pad_d_back - (p.kd - 1);
+    c.ok = true;
+    for (int i = 0; i < 3; ++i)
+        if (c.lo[i] < -16 || c.lo[i] > 15 || c.hi[i] < -16 || c.hi[i] > 15) c.ok = false;
+    return c;
+}
+
 template <typename T>
 cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, const float *b,
                             void *y, cudaStream_t s) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
-    if (!encode) return cudaErrorInvalidValue;
+    PFN_cuTensorMapEncodeIm2col_v12000 encode_im2col = get_encode_im2col();
+    if (!encode || !encode_im2col) return cudaErrorInvalidValue;
     DevInfo info;
     cudaError_t e = dev_info(&info);
     if (e != cudaSuccess) return e;
-    bool single_tile = false;
-    const TileGeom g = choose_geom(p, info.sms, &single_tile);
+    const TileGeom g = choose_geom(p, info.sms);
+    if (g.NP == 0) return cudaErrorInvalidValue;
     constexpr bool split = TcElt<T>::kSplit;
     constexpr int blk = TcElt<T>::kBlk;
     constexpr cuuint64_t elt = sizeof(T);
@@ -847,40 +852,28 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     const CUtensorMapDataType dt = split ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                          : (p.dtype == GBCONV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    const int64_t P = out_pixels(p);
 
     alignas(64) CUtensorMap tmX, tmW, tmY;
     std::memset(&tmY, 0, sizeof(tmY));
     const int Cs = split ? tc_split_half(p.C) : 0;
-    bool x_paired = false;
-    if (split && p.D == 1 && p.pad_d == 0) {
-        // fp32 conv2d: x as {Cs, W, H, 2, N}, the half axis Cs channels apart
-        // inside a row, so one box {32, BW s, BH s, 2, 1} lands as [x_hi | x_lo].
-        const cuuint64_t dims[5] = {(cuuint64_t)Cs, (cuuint64_t)p.W, (cuuint64_t)p.H, 2, (cuuint64_t)p.N};
-        const cuuint64_t strides[4] = {(cuuint64_t)Cp * elt, (cuuint64_t)Cp * elt * p.W, (cuuint64_t)Cs * elt,
-                                       (cuuint64_t)Cp * elt * p.W * p.H};
-        const cuuint32_t box[5] = {(cuuint32_t)blk, (cuuint32_t)(g.BW * p.stride), (cuuint32_t)(g.BH * p.stride), 2,
-                                   1};
-        const cuuint32_t es[5] = {1, (cuuint32_t)p.stride, (cuuint32_t)p.stride, 1, 1};
-        x_paired = encode(&tmX, dt, 5, const_cast<void *>(xc), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-    }
-    if (!x_paired) {
-        // Channels-last input as {Cp, W, H, D, N}; a box is one 128-byte K
-        // block of channels of one tile's (shifted) pixels; the conv stride is
-        // the element stride.
+    {
+        // Channels-last input as {Cp, W, H, D, N}, read in im2col mode: a load
+        // is NP consecutive output pixels x one 128-byte K block of channels,
+        // each pixel taken at its stride-spaced position shifted by the tap;
+        // taps reaching outside the input read zeros (the padding).
+        const Corners c = im2col_corners(p);
+        if (!c.ok) return cudaErrorInvalidValue;
         const cuuint64_t dims[5] = {(cuuint64_t)Cp, (cuuint64_t)p.W, (cuuint64_t)p.H,
                                     (cuuint64_t)p.D, (cuuint64_t)p.N};
         const cuuint64_t strides[4] = {(cuuint64_t)Cp * elt, (cuuint64_t)Cp * elt * p.W,
                                        (cuuint64_t)Cp * elt * p.W * p.H,
                                        (cuuint64_t)Cp * elt * p.W * p.H * p.D};
-        const cuuint32_t box[5] = {(cuuint32_t)blk, (cuuint32_t)(g.BW * p.stride),
-                                   (cuuint32_t)(g.BH * p.stride), 1, 1};
-        const cuuint32_t es[5] = {1, (cuuint32_t)p.stride, (cuuint32_t)p.stride, 1, 1};
-        if (encode(&tmX, dt, 5, const_cast<void *>(xc), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        const cuuint32_t es[5] = {1, (cuuint32_t)p.stride, (cuuint32_t)p.stride,
+                                  (cuuint32_t)(p.ndim == 3 ? p.stride : 1), 1};
+        if (encode_im2col(&tmX, dt, 5, const_cast<void *>(xc), dims, strides, c.lo, c.hi, (cuuint32_t)blk,
+                          (cuuint32_t)g.NP, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     if (split) {
@@ -912,75 +905,64 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
     a.y = y;
     a.OC = p.OC; a.OD = p.OD; a.OH = p.OH; a.OW = p.OW;
     a.k = p.k; a.pad = p.pad; a.pad_d = p.pad_d; a.stride = p.stride;
-    a.BW = g.BW; a.BH = g.BH; a.NP = g.NP;
-    a.tiles_w = (p.OW + g.BW - 1) / g.BW;
-    a.tiles_h = (p.OH + g.BH - 1) / g.BH;
+    a.out_vol = p.out_vol;
+    a.P = P;
+    a.NP = g.NP;
     a.oc_tiles = (p.OC + kTileOc - 1) / kTileOc;
-    const int64_t num_tiles = (int64_t)p.N * p.OD * a.tiles_h * a.tiles_w * a.oc_tiles;
+    const int64_t num_tiles = (P + g.NP - 1) / g.NP * a.oc_tiles;
     a.num_tiles = (int)num_tiles;
     a.cs = Cs;
-    a.x_paired = x_paired ? 1 : 0;
-    // x_lo: right after x_hi in a paired box; 1024-aligned when it is its own box.
-    a.xlo_off = x_paired ? 128u * (uint32_t)(g.BW * g.BH) : 128u * (uint32_t)((g.BW * g.BH + 7) / 8 * 8);
+    a.xlo_off = 128u * (uint32_t)g.NP;
     a.cblocks = split ? Cs / blk : (Cp + blk - 1) / blk;
     a.ksteps = p.taps * a.cblocks;
     a.stages = g.stages;
     a.relu = p.act == GBCONV_ACT_RELU;
-    a.vec_store = !split && (p.OW % 8 == 0) && (g.BW % 8 == 0) && (((uintptr_t)y % 16) == 0);
+    a.vec_store = !split && (p.out_vol % 8 == 0) && (((uintptr_t)y % 16) == 0);
     a.cl = p.cl;
     a.pair_store = !split && (p.OC % 2 == 0) && (((uintptr_t)y % 4) == 0);
     {
-        // Output as {OW, OH, OD, OC, N} (NCHW/NCDHW) or {OC, OW, OH, OD, N}
-        // (channels-last); a box is 32 pixels x 32 channels. Rows and the base
-        // 16-byte aligned, and for NCHW every box's first pixel on 16 bytes.
+        // Output views for 32 x 32 TMA tensor stores (rows and base 16-byte
+        // aligned; coordinates within int32): NC(D)HW as {out_vol, OC, N}
+        // (a chunk's 32 pixels are consecutive in one image's channel
+        // plane), channels-last as {OC, P} (32 consecutive pixel rows).
         const int a16 = 16 / (int)elt;
         const bool ok = ((uintptr_t)y % 16 == 0) &&
-                        (p.cl ? p.OC % a16 == 0 : (p.OW % a16 == 0 && g.BW % a16 == 0));
+                        (p.cl ? (p.OC % a16 == 0 && P < 0x7FFFFFFF)
+                              : (p.out_vol % a16 == 0 && p.out_vol < 0x7FFFFFFF));
         if (ok) {
-            const cuuint64_t e = elt;
-            cuuint64_t dims[5], strides[4];
-            cuuint32_t box[5];
+            const CUtensorMapSwizzle sw = split ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
             if (p.cl) {
-                const cuuint64_t d5[5] = {(cuuint64_t)p.OC, (cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.OD,
-                                          (cuuint64_t)p.N};
-                const cuuint32_t b5[5] = {32, 32, 1, 1, 1};
-                std::memcpy(dims, d5, sizeof(d5));
-                std::memcpy(box, b5, sizeof(b5));
+                const cuuint64_t dims[2] = {(cuuint64_t)p.OC, (cuuint64_t)P};
+                const cuuint64_t strides[1] = {(cuuint64_t)p.OC * elt};
+                const cuuint32_t box[2] = {32, 32};
+                const cuuint32_t es[2] = {1, 1};
+                a.tma_store = encode(&tmY, dt, 2, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+                              CUDA_SUCCESS;
             } else {
-                const cuuint64_t d5[5] = {(cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.OD, (cuuint64_t)p.OC,
-                                          (cuuint64_t)p.N};
-                const cuuint32_t b5[5] = {32, 1, 1, 32, 1};
-                std::memcpy(dims, d5, sizeof(d5));
-                std::memcpy(box, b5, sizeof(b5));
+                const cuuint64_t dims[3] = {(cuuint64_t)p.out_vol, (cuuint64_t)p.OC, (cuuint64_t)p.N};
+                const cuuint64_t strides[2] = {(cuuint64_t)p.out_vol * elt, (cuuint64_t)p.out_vol * p.OC * elt};
+                const cuuint32_t box[3] = {32, 32, 1};
+                const cuuint32_t es[3] = {1, 1, 1};
+                a.tma_store = encode(&tmY, dt, 3, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+                              CUDA_SUCCESS;
             }
-            cuuint64_t st = e;
-            for (int i = 0; i < 4; ++i) {
-                st *= dims[i];
-                strides[i] = st;
-            }
-            const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-            a.tma_store = encode(&tmY, dt, 5, y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                 split ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                                 CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
     }
     a.idesc = split ? make_idesc_tf32(kTileOc, g.NP) : make_idesc(kTileOc, g.NP, p.dtype == GBCONV_BF16);
-    a.tx_bytes = (split ? 2u : 1u) * (kWStageBytes + 128u * (uint32_t)(g.BW * g.BH));
-    {
-        // Accumulator 1's last 32-column epilogue read may run past 2 * NP.
-        const int last = g.NP + (g.BW * g.BH + kColChunk - 1) / kColChunk * kColChunk;
-        a.tmem_cols = tmem_cols_for(last > 2 * g.NP ? last : 2 * g.NP);
-    }
+    // every load is NP pixel rows of 128 B (zero-filled outside the input)
+    a.tx_bytes = (split ? 2u : 1u) * (kWStageBytes + 128u * (uint32_t)g.NP);
+    a.tmem_cols = tmem_cols_for(2 * g.NP);
     const double cyc = (double)wait_limit_ns() * (double)info.clock_khz * 1e-6;
     a.wait_limit_cycles = cyc > 9.0e18 ? (long long)9e18 : (long long)cyc;
 
-    a.single_tile = single_tile ? 1 : 0;
+    a.single_tile = g.single_tile ? 1 : 0;
     // Only when x is read in place: behind the layout pass the weights alone
     // measured no faster.
     a.prefetch = tc_cl_direct(p) ? 1 | (p.w_layout == GBCONV_W_PACKED ? 2 : 0) : 0;
     a.in_w = p.W; a.in_h = p.H; a.in_d = p.D;
-    const size_t smem = smem_bytes(g, p, single_tile);
+    const size_t smem = smem_bytes(g, p);
     auto kern = igemm_tc_kernel<T>;
     static std::atomic<uint64_t> attr_done{0};   // one bit per device
     int dev = 0;
@@ -991,6 +973,11 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
         attr_done.fetch_or(1ull << (dev & 63));
     }
     const int grid = num_tiles < info.sms ? (int)num_tiles : info.sms;
+    if (log_enabled())
+        log_line("igemm_tc_kernel<%s> grid=%d block=%d smem=%zu tiles=%lld pixels_per_tile=%d oc_tiles=%d "
+                 "stages=%d ksteps=%d store=%s%s", split ? "tf32x3" : (p.dtype == GBCONV_BF16 ? "bf16" : "f16"),
+                 grid, kThreads, smem, (long long)num_tiles, g.NP, a.oc_tiles, g.stages, a.ksteps,
+                 a.tma_store ? "tma" : "registers", g.single_tile ? " staging_in_ring" : "");
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, tmX, tmW, tmY, a);
 }
 
@@ -1189,12 +1176,11 @@ cudaError_t launch_prep_split(const Problem &p, const void *w, void *wp, const v
 }  // namespace
 
 bool tc_supported(const Problem &p) {
-    // The SM count only shapes the row tiling, not whether the boxes fit.
+    // The SM count only shapes the tiling, not whether a tile fits.
     const TileGeom g = choose_geom(p, 152);
-    const int64_t mtiles = (int64_t)p.N * p.OD * ((p.OH + g.BH - 1) / g.BH) *
-                           ((p.OW + g.BW - 1) / g.BW) * ((p.OC + kTileOc - 1) / kTileOc);
-    return g.BW * p.stride <= 256 && g.BH * p.stride <= 256 && mtiles < 0x7FFFFFFF &&
-           g.stages >= 2 && p.N <= 65535;
+    if (g.NP == 0 || !im2col_corners(p).ok) return false;
+    const int64_t tiles = (out_pixels(p) + g.NP - 1) / g.NP * ((p.OC + kTileOc - 1) / kTileOc);
+    return tiles < 0x7FFFFFFF && out_pixels(p) < ((int64_t)1 << 40);
 }
 
 cudaError_t launch_igemm_tc(const Problem &p, const void *xc, const void *wp, const float *b,

@@ -86,7 +86,45 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// TMA load in im2col mode from a channels-last 5-D tensor {C, W, H, D, N}:
+// pixelsPerColumn consecutive output pixels (the tensor map's traversal walks
+// W, then H, then D, then N, each over the range its pixel-box corners allow,
+// by its element stride) of channelsPerPixel channels from channel c, each
+// pixel read at its traversal position plus the tap offsets (ow, oh, od).
+// (w, h, d, n) is the traversal position of the first pixel; positions
+// outside the tensor read as zero. Lands as one 128-byte row per pixel.
+__device__ __forceinline__ void tma_load_im2col_5d(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int c,
+                                                   int w, int h, int d, int n, uint16_t ow, uint16_t oh,
+                                                   uint16_t od) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], {%8, %9, %10};" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(d), "r"(n), "h"(ow), "h"(oh),
+        "h"(od)
+        : "memory");
+}
+// The same box as an L2 prefetch (a hint: no shared-memory destination, no
+// barrier).
+__device__ __forceinline__ void tma_prefetch_l2_im2col_5d(const CUtensorMap *tm, int c, int w, int h, int d, int n,
+                                                          uint16_t ow, uint16_t oh, uint16_t od) {
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.im2col [%0, {%1, %2, %3, %4, %5}], {%6, %7, %8};" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c), "r"(w), "r"(h), "r"(d), "r"(n), "h"(ow), "h"(oh), "h"(od)
+                 : "memory");
+}
 // Tensor store from shared memory (bulk group), its commit and waits.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap *tm, uint32_t src, int c0, int c1, int c2,
                                              int c3) {
     asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
