@@ -572,13 +572,14 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 }
 
 // x [N][C][S] -> xc [N][S][Cp], zero in channels C..Cp-1 (S = D*H*W).
-// A CTA moves 64 channels x 128 positions (16 KB) through shared memory:
-// loads are 16-byte vectors along a channel's positions (16 lanes = 256
-// contiguous bytes), stores 16-byte vectors of 8 channels (8 lanes = one
-// position's 128 contiguous bytes). The shared tile keeps a channel's row of
-// positions in 16-byte chunks whose index is XOR-ed with (channel / 8), so
-// the column reads of the store phase hit 16 different banks per warp.
-constexpr int kClC = 64, kClS = 128;
+// A CTA moves 64 channels x 256 positions (32 KB of 16-bit values) through
+// shared memory, all of its loads in flight at once (8 per thread): loads
+// are 16-byte vectors along a channel's positions (32 lanes = 512 contiguous
+// bytes), stores 16-byte vectors of 8 channels (8 lanes = one position's 128
+// contiguous bytes). The shared tile keeps a channel's row of positions in
+// 16-byte chunks whose index is XOR-ed with (channel / 8) % 8, so the column
+// reads of the store phase hit 16 different banks per warp.
+constexpr int kClC = 64, kClS = 256;
 template <typename T, bool VEC>
 __device__ __forceinline__ void to_channels_last_block(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp,
                                                        int64_t S, int bx, int by, int bz, T (*tile)[kClS]) {
@@ -587,24 +588,32 @@ __device__ __forceinline__ void to_channels_last_block(const T *__restrict__ x, 
     const int n = bz;
     const T *xn = x + (int64_t)n * C * S;
     T *xcn = xc + (int64_t)n * S * Cp;
+    constexpr int kIter = kClC * kClS / 8 / 256;
+    uint4 buf[kIter];
 #pragma unroll
-    for (int i = 0; i < kClC * kClS / 8 / 256; ++i) {
+    for (int i = 0; i < kIter; ++i) {
         const int v = threadIdx.x + 256 * i;
-        const int cl = v / 16, p8 = v % 16;
+        const int cl = v / (kClS / 8), p8 = v % (kClS / 8);
         const int cc = c0 + cl;
         const int64_t s = s0 + p8 * 8;
-        T *dst = &tile[cl][(p8 ^ ((cl >> 3) & 7)) * 8];
         if (VEC && cc < C && s + 8 <= S) {
-            *reinterpret_cast<uint4 *>(dst) = __ldg(reinterpret_cast<const uint4 *>(xn + (int64_t)cc * S + s));
+            buf[i] = __ldg(reinterpret_cast<const uint4 *>(xn + (int64_t)cc * S + s));
         } else {
+            alignas(16) T e[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                dst[j] = (cc < C && s + j < S) ? xn[(int64_t)cc * S + s + j] : T(0.0f);
+            for (int j = 0; j < 8; ++j) e[j] = (cc < C && s + j < S) ? xn[(int64_t)cc * S + s + j] : T(0.0f);
+            buf[i] = *reinterpret_cast<const uint4 *>(e);
         }
+    }
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int v = threadIdx.x + 256 * i;
+        const int cl = v / (kClS / 8), p8 = v % (kClS / 8);
+        *reinterpret_cast<uint4 *>(&tile[cl][(p8 ^ ((cl >> 3) & 7)) * 8]) = buf[i];
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kClC * kClS / 8 / 256; ++i) {
+    for (int i = 0; i < kIter; ++i) {
         const int v = threadIdx.x + 256 * i;
         const int cch = v % 8, pos = v / 8;
         const int cc = c0 + cch * 8;
@@ -619,7 +628,7 @@ __device__ __forceinline__ void to_channels_last_block(const T *__restrict__ x, 
     }
 }
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S) {
     __shared__ __align__(16) T tile[kClC][kClS];
     pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
@@ -627,36 +636,96 @@ to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int 
 }
 
 // wp[tap][oc][cp] = w[oc][c][tap] for c < C, zero for C <= cp < Cp. A CTA
-// handles one output channel, 64 channels and up to 32 taps: the taps of its
-// channels are tn-element runs of w (one contiguous run of 64 * tn elements
-// when all taps fit), read with consecutive threads on consecutive elements
-// into shared memory; each tap's 64 channels then leave as one 128-byte run
-// of wp.
-constexpr int kPkC = 64, kPkT = 32;
+// handles ocpb (1 to 8, about 512 16-byte vectors' worth: pack_oc_block)
+// output channels, 64 channels and up to 32 taps. When all taps
+// fit and the block is whole, each output channel's part of w is one
+// contiguous run of 64 * taps elements, read as 16-byte vectors; a thread
+// issues all of its loads (at most 8) before it writes any to shared memory,
+// so the CTA waits for one memory round trip. Other blocks read element by
+// element in batches of 8 loads. Each (tap, output channel) pair's 64
+// channels then leave as one 128-byte run of wp.
+constexpr int kPkC = 64, kPkT = 32, kPkOc = 8;
+// Output channels per pack block: the largest power of two up to 8 whose
+// block is at most 512 vectors of 8 elements (two loads per thread).
+inline int pack_oc_block(int taps) {
+    const int tn = taps < kPkT ? taps : kPkT;
+    int o = kPkOc;
+    while (o > 1 && o * kPkC * tn / 8 > 512) o /= 2;
+    return o;
+}
 template <typename T>
 __device__ __forceinline__ void pack_tc_block(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp,
-                                              int taps, int oc, int by, int bz, T (*tile)[kPkT + 1]) {
-    const int c0 = by * kPkC, t0 = bz * kPkT;
+                                              int taps, int ocpb, int bx, int by, int bz,
+                                              T (*tile)[kPkC][kPkT + 1]) {
+    static_assert(sizeof(T) == 2, "16-bit weights");
+    const int oc0 = bx * ocpb, c0 = by * kPkC, t0 = bz * kPkT;
     const int tn = taps - t0 < kPkT ? taps - t0 : kPkT;
-    const T *src = w + (int64_t)oc * C * taps + t0;
-    for (int e = threadIdx.x; e < kPkC * tn; e += blockDim.x) {
-        const int cl = e / tn, tl = e - cl * tn;
-        const int c = c0 + cl;
-        tile[cl][tl] = c < C ? src[(int64_t)c * taps + tl] : T(0.0f);
+    const bool vec = t0 == 0 && tn == taps && c0 + kPkC <= C && oc0 + ocpb <= OC &&
+                     ((int64_t)C * taps) % 8 == 0 && ((uintptr_t)w % 16) == 0;
+    if (vec) {
+        const int vpr = kPkC * taps / 8;                      // vectors per output channel's run
+        constexpr int kMaxV = kPkOc * kPkC * kPkT / 8 / 256;  // 8
+        uint4 buf[kMaxV];
+#pragma unroll
+        for (int k = 0; k < kMaxV; ++k) {
+            const int v = threadIdx.x + 256 * k;
+            if (v < ocpb * vpr) {
+                const int o = v / vpr, r = v - o * vpr;
+                buf[k] = __ldg(reinterpret_cast<const uint4 *>(w + ((int64_t)(oc0 + o) * C + c0) * taps) + r);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxV; ++k) {
+            const int v = threadIdx.x + 256 * k;
+            if (v < ocpb * vpr) {
+                const int o = v / vpr, r = v - o * vpr;
+                const T *e = reinterpret_cast<const T *>(&buf[k]);
+                int j = r * 8;
+                int cl = j / taps, tl = j - cl * taps;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    tile[o][cl][tl] = e[q];
+                    if (++tl == taps) { tl = 0; ++cl; }
+                }
+            }
+        }
+    } else {
+        const int per_oc = kPkC * tn;
+        for (int e0 = 0; e0 < ocpb * per_oc; e0 += 8 * 256) {
+            T v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int e = e0 + 256 * k + threadIdx.x;
+                const int o = e / per_oc, r = e - o * per_oc;
+                const int cl = r / tn, tl = r - cl * tn;
+                const int oc = oc0 + o, c = c0 + cl;
+                v[k] = (e < ocpb * per_oc && oc < OC && c < C) ? w[((int64_t)oc * C + c) * taps + t0 + tl] : T(0.0f);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int e = e0 + 256 * k + threadIdx.x;
+                if (e < ocpb * per_oc) {
+                    const int o = e / per_oc, r = e - o * per_oc;
+                    const int cl = r / tn, tl = r - cl * tn;
+                    tile[o][cl][tl] = v[k];
+                }
+            }
+        }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < kPkC * tn; e += blockDim.x) {
-        const int tl = e / kPkC, cl = e % kPkC;
-        const int cp = c0 + cl;
-        if (cp < Cp) wp[((int64_t)(t0 + tl) * OC + oc) * Cp + cp] = tile[cl][tl];
+    for (int e = threadIdx.x; e < tn * ocpb * kPkC; e += blockDim.x) {
+        const int cl = e % kPkC, r = e / kPkC;
+        const int o = r % ocpb, tl = r / ocpb;
+        const int oc = oc0 + o, cp = c0 + cl;
+        if (oc < OC && cp < Cp) wp[((int64_t)(t0 + tl) * OC + oc) * Cp + cp] = tile[o][cl][tl];
     }
 }
 template <typename T>
-__global__ void __launch_bounds__(256)
-pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp, int taps) {
-    __shared__ T tile[kPkC][kPkT + 1];
+__global__ void __launch_bounds__(256, 4)
+pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp, int taps, int ocpb) {
+    __shared__ T tile[kPkOc][kPkC][kPkT + 1];
     pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
-    pack_tc_block<T>(w, wp, OC, C, Cp, taps, blockIdx.x, blockIdx.y, blockIdx.z, tile);
+    pack_tc_block<T>(w, wp, OC, C, Cp, taps, ocpb, blockIdx.x, blockIdx.y, blockIdx.z, tile);
 }
 
 // CTA b of a grid that holds npk CTAs of one pass and nlay of another, the
@@ -673,23 +742,29 @@ __device__ __forceinline__ int prep_block_index(int b, int npk, int nlay, bool *
 }
 
 // Both passes in front of the GEMM when the weights come as OIHW: npk CTAs
-// do the weight-pack blocks (grid OC x pky x pkz, x fastest) and nlay the
+// do the weight-pack blocks (grid pkx x pky x pkz, x fastest) and nlay the
 // layout blocks (grid clx x cly x N). The passes touch disjoint memory, so
 // one grid runs them side by side and the GEMM waits on one launch.
+template <typename T>
+constexpr size_t prep_tile_bytes() {
+    return sizeof(T) * kClC * kClS > sizeof(T) * kPkOc * kPkC * (kPkT + 1) ? sizeof(T) * kClC * kClS
+                                                                          : sizeof(T) * kPkOc * kPkC * (kPkT + 1);
+}
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 prep_tc_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S, int clx, int cly,
-               const T *__restrict__ w, T *__restrict__ wp, int OC, int taps, int pky, int npk, int nlay) {
-    __shared__ __align__(16) T tile[kClC][kClS];
-    static_assert(sizeof(T) * kPkC * (kPkT + 1) <= sizeof(T) * kClC * kClS, "pack tile fits the layout tile");
+               const T *__restrict__ w, T *__restrict__ wp, int OC, int taps, int ocpb, int pkx, int pky, int npk,
+               int nlay) {
+    __shared__ __align__(16) unsigned char tile[prep_tile_bytes<T>()];
     pdl_wait();   // dependents start when this grid completes
     bool pack;
     const int q = prep_block_index(blockIdx.x, npk, nlay, &pack);
     if (pack)
-        pack_tc_block<T>(w, wp, OC, C, Cp, taps, q % OC, (q / OC) % pky, q / (OC * pky),
-                         reinterpret_cast<T (*)[kPkT + 1]>(&tile[0][0]));
+        pack_tc_block<T>(w, wp, OC, C, Cp, taps, ocpb, q % pkx, (q / pkx) % pky, q / (pkx * pky),
+                         reinterpret_cast<T (*)[kPkC][kPkT + 1]>(tile));
     else
-        to_channels_last_block<T, VEC>(x, xc, C, Cp, S, q % clx, (q / clx) % cly, q / (clx * cly), tile);
+        to_channels_last_block<T, VEC>(x, xc, C, Cp, S, q % clx, (q / clx) % cly, q / (clx * cly),
+                                       reinterpret_cast<T (*)[kClS]>(tile));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -985,10 +1060,10 @@ cudaError_t launch_tc_typed(const Problem &p, const void *xc, const void *wp, co
 
 // fp32 on the tensor cores: x -> xs [N][S][2 Cs] with xs[..][c] = hi(x) and
 // xs[..][Cs + c] = lo(x) = x - hi(x) for c < C, zero up to Cs (S = D*H*W).
-// From NC(D)HW a CTA moves 32 channels x 128 positions through a padded
+// From NC(D)HW a CTA moves 32 channels x 256 positions through a padded
 // shared tile (loads along positions, stores along channels); from
 // channels-last x each thread splits one element in place of the copy.
-constexpr int kSpC = 32, kSpS = 128;
+constexpr int kSpC = 32, kSpS = 256;
 template <bool VEC>
 __device__ __forceinline__ void split_nchw_block(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs,
                                                  int64_t S, int bx, int by, int bz, float (*tile)[kSpS + 1]) {
@@ -997,8 +1072,13 @@ __device__ __forceinline__ void split_nchw_block(const float *__restrict__ x, fl
     const int n = bz;
     const float *xn = x + (int64_t)n * C * S;
     // Loads: 4 consecutive positions of one channel per thread (16-byte
-    // vectors when S is a multiple of 4 and x 16-byte aligned).
-    for (int e = threadIdx.x; e < kSpC * kSpS / 4; e += blockDim.x) {
+    // vectors when S is a multiple of 4 and x 16-byte aligned), all of a
+    // thread's loads in flight before any is stored.
+    constexpr int kIter = kSpC * kSpS / 4 / 256;
+    float4 buf[kIter];
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int e = threadIdx.x + 256 * i;
         const int cl = e / (kSpS / 4), sl = (e % (kSpS / 4)) * 4;
         const int c = c0 + cl;
         const int64_t sp = s0 + sl;
@@ -1013,16 +1093,24 @@ __device__ __forceinline__ void split_nchw_block(const float *__restrict__ x, fl
                 if (sp + 3 < S) v.w = __ldg(xn + (int64_t)c * S + sp + 3);
             }
         }
-        tile[cl][sl] = v.x;
-        tile[cl][sl + 1] = v.y;
-        tile[cl][sl + 2] = v.z;
-        tile[cl][sl + 3] = v.w;
+        buf[i] = v;
+    }
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int e = threadIdx.x + 256 * i;
+        const int cl = e / (kSpS / 4), sl = (e % (kSpS / 4)) * 4;
+        tile[cl][sl] = buf[i].x;
+        tile[cl][sl + 1] = buf[i].y;
+        tile[cl][sl + 2] = buf[i].z;
+        tile[cl][sl + 3] = buf[i].w;
     }
     __syncthreads();
     // Stores: 4 consecutive channels of one position per thread, hi and lo
     // halves as two 16-byte vectors (Cs is a multiple of 32).
     float *xsn = xs + (int64_t)n * S * 2 * Cs;
-    for (int e = threadIdx.x; e < kSpC * kSpS / 4; e += blockDim.x) {
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+        const int e = threadIdx.x + 256 * i;
         const int sl = e / (kSpC / 4), cl = (e % (kSpC / 4)) * 4;
         const int64_t sp = s0 + sl;
         if (sp < S) {
@@ -1135,9 +1223,11 @@ cudaError_t launch_cl_typed(const Problem &p, const void *x, void *xc, cudaStrea
 template <typename T>
 cudaError_t launch_pack_tc_typed(const Problem &p, const void *w, void *wp, cudaStream_t s) {
     const int Cp = tc_cpad(p.C);
-    dim3 grid((unsigned)p.OC, (unsigned)((Cp + kPkC - 1) / kPkC), (unsigned)((p.taps + kPkT - 1) / kPkT));
+    const int ocpb = pack_oc_block(p.taps);
+    dim3 grid((unsigned)((p.OC + ocpb - 1) / ocpb), (unsigned)((Cp + kPkC - 1) / kPkC),
+              (unsigned)((p.taps + kPkT - 1) / kPkT));
     return launch_pdl(pack_tc_kernel<T>, grid, dim3(256), 0, s, static_cast<const T *>(w), static_cast<T *>(wp),
-                      p.OC, p.C, Cp, p.taps);
+                      p.OC, p.C, Cp, p.taps, ocpb);
     return cudaGetLastError();
 }
 
@@ -1146,15 +1236,16 @@ cudaError_t launch_prep_tc_typed(const Problem &p, const void *w, void *wp, cons
     const int Cp = tc_cpad(p.C);
     const int64_t S = p.in_vol;
     const int64_t clx = (S + kClS - 1) / kClS, cly = (Cp + kClC - 1) / kClC;
-    const int64_t pky = (Cp + kPkC - 1) / kPkC, pkz = (p.taps + kPkT - 1) / kPkT;
-    const int64_t npk = (int64_t)p.OC * pky * pkz, nlay = clx * cly * p.N;
+    const int ocpb = pack_oc_block(p.taps);
+    const int64_t pkx = (p.OC + ocpb - 1) / ocpb, pky = (Cp + kPkC - 1) / kPkC, pkz = (p.taps + kPkT - 1) / kPkT;
+    const int64_t npk = pkx * pky * pkz, nlay = clx * cly * p.N;
     const int64_t total = npk + nlay;
     if (total > 0x7FFFFFFF) return cudaErrorNotSupported;   // caller falls back to two launches
     const bool vec = (S % 8 == 0) && ((uintptr_t)x % 16 == 0);
     auto kern = vec ? prep_tc_kernel<T, true> : prep_tc_kernel<T, false>;
     return launch_pdl(kern, dim3((unsigned)total), dim3(256), 0, s, static_cast<const T *>(x), static_cast<T *>(xc),
                       p.C, Cp, S, (int)clx, (int)cly, static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.taps,
-                      (int)pky, (int)npk, (int)nlay);
+                      ocpb, (int)pkx, (int)pky, (int)npk, (int)nlay);
 }
 
 cudaError_t launch_prep_split(const Problem &p, const void *w, void *wp, const void *x, void *xs, cudaStream_t s) {
