@@ -270,7 +270,43 @@ __device__ __forceinline__ void stem_epilogue(const StemTcArgs &a, uint32_t tlan
     }
 }
 
-template <int C, bool TMA, bool ATM>
+// This thread's T taps, pixel (r, j) of a TMA tile, from a halo buffer
+// (shared memory, byte offset hoff from the dynamic shared-memory base).
+template <int C>
+__device__ __forceinline__ void stem_halo_taps(const StemTcArgs &a, const uint8_t *smem_raw, uint32_t hoff, int r,
+                                               int j, bool pair_taps, float (&xv)[C * 9]) {
+    const float *h = reinterpret_cast<const float *>(smem_raw + hoff);
+    const int s = a.stride;
+    if (pair_taps) {
+        // Stride 2, odd hd: taps 1 and 2 of a row sit at an even column, so
+        // one 8-byte load fetches both.
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+#pragma unroll
+            for (int ky = 0; ky < 3; ++ky) {
+                const float *hr = h + (c * a.hbh + r * 2 + ky) * a.hbw + j * 2 + a.hd;
+                const float2 t12 = *reinterpret_cast<const float2 *>(hr + 1);
+                xv[(c * 3 + ky) * 3] = hr[0];
+                xv[(c * 3 + ky) * 3 + 1] = t12.x;
+                xv[(c * 3 + ky) * 3 + 2] = t12.y;
+            }
+    } else {
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+#pragma unroll
+            for (int ky = 0; ky < 3; ++ky) {
+                const float *hr = h + (c * a.hbh + r * s + ky) * a.hbw + j * s + a.hd;
+#pragma unroll
+                for (int kx = 0; kx < 3; ++kx) xv[(c * 3 + ky) * 3 + kx] = hr[kx];
+            }
+    }
+}
+
+// Overlapped tile loop (TMA tiles, pixel operand in TMEM, OCP <= 32): the
+// accumulator row fits in registers.
+constexpr int kStemOvlMaxOcp = 32;
+
+template <int C, bool TMA, bool ATM, bool OVL>
 __global__ void __launch_bounds__(kStemPxThreads * kStemMaxGroups, 1)
 stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
                  const StemTcArgs a) {
@@ -392,7 +428,102 @@ stem_tf32_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
 
     uint32_t mphase = 0;
-    if (TMA) {
+    if constexpr (TMA && ATM && OVL) {
+        // A group reads tile k's accumulator into registers, builds tile
+        // k+1's operand and issues its MMAs, and only then stages and stores
+        // tile k: the next tile's MMAs run under this tile's epilogue.
+        const int r = gtid / kStemTileW, j = gtid % kStemTileW;    // this thread's pixel in the tile
+        const bool pair_taps = a.stride == 2 && (a.hd & 1) && (a.hbw % 2 == 0);
+        const uint32_t stage = sA + a.stage_off;
+        const uint32_t stg = stage + (uint32_t)((r * kStemTileW + j) * 4);
+        // The operand of this group's tile number kk, from halo buffer kk & 1.
+        auto build = [&](int kk) {
+            const int hb = kk & 1;
+            const uint32_t hpar = (uint32_t)((kk >> 1) & 1);
+            const bool landed = warp_wait(barH + 8u * hb, hpar, a.wait_limit_cycles, abort_flag);
+            if (gtid == 0 && landed && halo_pending[hb] == 1u + hpar) halo_pending[hb] = 0;
+            stem_halo_taps<C>(a, smem_raw, sHalo + (uint32_t)hb * a.halo_bytes - raw, r, j, pair_taps, xv);
+            put_pixel_row<C, true>(sA, tA + lane_off, gtid, xv);
+        };
+        // After the group barrier that follows build(kk): the halo two tiles
+        // ahead into the buffer just read, then tile t's MMAs (nothing new
+        // once a wait has run out).
+        auto issue = [&](int kk, int t) {
+            if (gtid == 0 && !*abort_flag) {
+                const int hb = kk & 1;
+                const int ahead = t + 2 * tstep;
+                if (ahead < tend) {
+                    stem_load_halo(&tmX, a, ahead, sHalo + (uint32_t)hb * a.halo_bytes, barH + 8u * hb);
+                    halo_pending[hb] = 1u + (uint32_t)(((kk + 2) >> 1) & 1);
+                }
+                stem_mmas<KP, true>(tacc, tA, sA, sB, bchunk, a.idesc);
+                tc_commit(barM);
+                mma_pending = 1u + mphase;
+            }
+        };
+        if (active) {
+            build(0);
+            tc_fence_before();
+            named_barrier(1 + g, kStemPxThreads);          // operand written, halo buffer 0 read
+            tc_fence_after();
+            issue(0, tile);
+        }
+        for (int k = 0; active; ++k) {
+            const int next = tile + tstep;
+            const bool has_next = next < tend;
+            if (warp_wait(barM, mphase, a.wait_limit_cycles, abort_flag) && gtid == 0 && mma_pending == 1u + mphase)
+                mma_pending = 0;
+            mphase ^= 1u;
+            tc_fence_after();
+            float v[kStemOvlMaxOcp];
+#pragma unroll
+            for (int c0 = 0; c0 < kStemOvlMaxOcp; c0 += 16) {
+                if (c0 < a.ocp) {
+                    uint32_t hv[16], lv[16];
+                    tmem_ld16(tacc + lane_off + (uint32_t)c0, hv);
+                    tmem_ld16(tacc + lane_off + (uint32_t)(a.ocp + c0), lv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        v[c0 + e] = epilogue(__uint_as_float(hv[e]) + __uint_as_float(lv[e]), sBias[c0 + e], a.relu);
+                }
+            }
+            // Tile k's MMAs are done and its accumulator is in registers: the
+            // operand and the accumulator are free for tile k+1.
+            if (has_next) build(k + 1);
+            // The previous tile's output stores have read the staging tile.
+            if (gtid == 0) bulk_wait_read<0>();
+            tc_fence_before();
+            named_barrier(1 + g, kStemPxThreads);          // accumulator read, operand written, staging free
+            tc_fence_after();
+            if (has_next) issue(k + 1, next);
+            // Tile k's outputs: staging tile [oc][row][pixel], then TMA stores.
+#pragma unroll
+            for (int oc = 0; oc < kStemOvlMaxOcp; ++oc)
+                if (oc < a.ocp)
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stg + (uint32_t)(oc * kStemTileR * kStemTileW * 4)),
+                                 "f"(v[oc])
+                                 : "memory");
+            fence_proxy_async_shared();
+            named_barrier(1 + g, kStemPxThreads);
+            if (gtid == 0 && !*abort_flag) {
+                const StemTile st = stem_tile(a, tile);
+                const uint32_t box_bytes = (uint32_t)(a.ybox_c * kStemTileR * kStemTileW * 4);
+                for (int c0 = 0, bi = 0; c0 < a.OC; c0 += a.ybox_c, ++bi)
+                    tma_store_4d(&tmY, stage + (uint32_t)bi * box_bytes, st.ow0, st.oh0, c0, st.n);
+                bulk_commit_group();
+            }
+            if (!has_next) break;
+            tile = next;
+        }
+        if (gtid == 0) {
+            bulk_wait_read_all();
+            // After an abort a halo load may still be in flight: wait for it
+            // to land (it is the current phase of its buffer's barrier).
+            for (int k = 0; k < 2; ++k)
+                if (halo_pending[k]) wait_bounded(barH + 8u * k, halo_pending[k] - 1u, kDrainLimitCycles, nullptr);
+        }
+    } else if (TMA) {
         const int r = gtid / kStemTileW, j = gtid % kStemTileW;    // this thread's pixel in the tile
         const int s = a.stride;
         const bool pair_taps = s == 2 && (a.hd & 1) && (a.hbw % 2 == 0);
@@ -641,15 +772,19 @@ cudaError_t launch_stem_tf32_c(const Problem &p, const float *x, const float *w,
     while (cols < (uint32_t)G * a.group_cols) cols *= 2;
     a.tmem_cols = cols;
     const size_t smem = stem_tc_smem_bytes(a, C, tma, G);
-    auto kern = tma ? (atm ? stem_tf32_kernel<C, true, true> : stem_tf32_kernel<C, true, false>)
-                    : (atm ? stem_tf32_kernel<C, false, true> : stem_tf32_kernel<C, false, false>);
+    // Overlapped tile loop when the accumulator row fits in registers.
+    const bool ovl = tma && atm && a.ocp <= kStemOvlMaxOcp;
+    auto kern = tma ? (atm ? (ovl ? stem_tf32_kernel<C, true, true, true> : stem_tf32_kernel<C, true, true, false>)
+                           : stem_tf32_kernel<C, true, false, false>)
+                    : (atm ? stem_tf32_kernel<C, false, true, false> : stem_tf32_kernel<C, false, false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // One CTA per SM (a kernel that uses TMEM is resident once per SM).
     const int ctas = (a.tiles + G - 1) / G;
     const int grid = ctas < info.sms ? ctas : info.sms;
     if (log_enabled())
-        log_line("stem_tf32_kernel<C=%d> grid=%d block=%d smem=%zu groups=%d tiles=%d operand=%s io=%s", C, grid,
-                 kStemPxThreads * G, smem, G, a.tiles, atm ? "tmem" : "smem", tma ? "tma" : "plain");
+        log_line("stem_tf32_kernel<C=%d> grid=%d block=%d smem=%zu groups=%d tiles=%d operand=%s io=%s%s", C, grid,
+                 kStemPxThreads * G, smem, G, a.tiles, atm ? "tmem" : "smem", tma ? "tma" : "plain",
+                 ovl ? " overlapped" : "");
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kStemPxThreads * G), smem, s, tmX, tmY, a);
 }
