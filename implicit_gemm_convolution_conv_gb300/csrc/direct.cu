@@ -60,6 +60,7 @@ direct_conv_kernel(const DirectArgs a) {
     const int KK = k * k;
 
     extern __shared__ float smem[];
+    pdl_wait();   // launched with programmatic dependent launch: global memory after the predecessor
     float *wsm = smem;                         // [CF * k * k][OCB]
     float *xs = smem + CF * KK * OCB;          // [CF][IHT][IWT]
 
@@ -180,8 +181,7 @@ cudaError_t launch_tile(const Problem &p, const DirectArgs &a0, cudaStream_t st)
     if (log_enabled())
         log_line("direct_conv_kernel grid=%ux%ux%u block=%d smem=%zu tile=%dx%d oc_block=%d", grid.x, grid.y,
                  grid.z, TL::NT, smem, TH, TW, OCB);
-    kern<<<grid, TL::NT, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(TL::NT), smem, st, a);
 }
 
 // Tile shapes: "wide" for >= 16 output channels, "narrow" otherwise.

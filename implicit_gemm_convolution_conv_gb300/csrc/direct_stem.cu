@@ -110,6 +110,11 @@ direct_stem_kernel(const StemArgs a) {
     constexpr int kTasks = (kRows * G::kChunks + 31) / 32;      // 16-byte chunks per lane
     __shared__ __align__(16) float halo[kWarps][kRing][kBuf];     // halo ring
 
+    // Programmatic dependent launch: the grid is one resident wave, so the
+    // next kernel in the stream may launch now; this one reads global memory
+    // only once its predecessor has completed.
+    pdl_launch_dependents();
+    pdl_wait();
     const int wid = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gw = blockIdx.x * kWarps + wid;
     const int ocb = gw % a.oc_blocks;
@@ -384,8 +389,7 @@ cudaError_t launch_stem_csp(const Problem &p, const StemArgs &a0, cudaStream_t s
     if (log_enabled())
         log_line("direct_stem_kernel grid=%d block=%d warps_per_oc_block=%d oc_blocks=%d pixel_tiles=%lld", grid,
                  kWarps * 32, a.warps_per_ocb, a.oc_blocks, (long long)a.pix_tiles);
-    kern<<<grid, kWarps * 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kWarps * 32), 0, s, a);
 }
 
 template <typename T, int C, int S, int PAD>
