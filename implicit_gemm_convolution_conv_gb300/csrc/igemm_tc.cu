@@ -370,9 +370,16 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const uint32_t ystage = sY + (uint32_t)(warp - 2) * 2u * TcElt<T>::kChunkBytes;
         int nst = 0;             // TMA stores this warp has issued
         int local = 0;
+        const long long n_img = a.P / a.out_vol;
         for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++local) {
             const TileCoord tc = tile_coord(a, t);
+            // the tile's first pixel within image tc.n's planes
+            const long long v_tile = tc.p0 - (long long)tc.n * a.out_vol;
             const int acc = local & 1;
+            const int oc = tc.oc0 + q * 32 + lane;
+            const bool oc_ok = oc < a.OC;
+            // the bias load's latency passes while the accumulator fills
+            const float bias = (a.b && oc_ok) ? __ldg(a.b + oc) : 0.0f;
             int ok = 0;
             if (lane == 0)
                 ok = wait_bounded(tfull0 + 8u * acc, (uint32_t)(local >> 1) & 1u, limit, abort_flag) ? 1 : 0;
@@ -382,9 +389,6 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 break;
             }
             tc_fence_after();
-            const int oc = tc.oc0 + q * 32 + lane;
-            const bool oc_ok = oc < a.OC;
-            const float bias = (a.b && oc_ok) ? __ldg(a.b + oc) : 0.0f;
             const bool odd = lane & 1;
             const int oc_even = oc - (odd ? 1 : 0);
             // One 32-pixel chunk, pixels pc .. pc + 31 of the (n, od, oh, ow)
@@ -395,9 +399,15 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 const long long pc = tc.p0 + (long long)ch * kColChunk;
                 if (pc >= a.P) return;
                 const int nv = a.P - pc < kColChunk ? (int)(a.P - pc) : kColChunk;
-                const long long n0 = pc / a.out_vol;
-                const long long v0 = pc - n0 * a.out_vol;
-                const bool one_image = v0 + kColChunk <= a.out_vol || n0 + 1 == a.P / a.out_vol;
+                // image n0 and plane position v0 of pixel pc, stepped from the
+                // tile's start (no 64-bit division per chunk)
+                long long n0 = tc.n, v0 = v_tile + (long long)ch * kColChunk;
+                if (!a.cl)
+                    while (v0 >= a.out_vol) {
+                        v0 -= a.out_vol;
+                        ++n0;
+                    }
+                const bool one_image = v0 + kColChunk <= a.out_vol || n0 + 1 == n_img;
                 // One box: a channels-last chunk always; an NC(D)HW chunk that
                 // lies in one image's planes (the tensor's end clips the last).
                 if (a.tma_store && (a.cl || one_image)) {
@@ -438,19 +448,24 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                       if (a.cl) {
                         // [pixel][channel] rows of 64 B; 16-byte unit u of row e
                         // sits at unit u ^ ((e >> 1) & 3) (64-byte swizzle).
+                        // All 16 exchanges first, then the stores: no store
+                        // waits behind a shuffle's latency.
                         const uint32_t cb = (uint32_t)(lane & ~1) * 2u;      // byte of channel pair
+                        uint32_t pk[kColChunk / 2];
 #pragma unroll
                         for (int e = 0; e < kColChunk; e += 2) {
                             const float v0f = epilogue(__uint_as_float(v[e]), bias, a.relu);
                             const float v1f = epilogue(__uint_as_float(v[e + 1]), bias, a.relu);
                             const float got = __shfl_xor_sync(0xffffffffu, odd ? v0f : v1f, 1);
                             const typename Storage<T>::Pair pr = Storage<T>::pack2(odd ? got : v0f, odd ? v1f : got);
+                            pk[e / 2] = *reinterpret_cast<const uint32_t *>(&pr);
+                        }
+#pragma unroll
+                        for (int e = 0; e < kColChunk; e += 2) {
                             const int row = e + (odd ? 1 : 0);
                             const uint32_t addr = buf + (uint32_t)row * 64u +
                                                   ((((cb >> 4) ^ (uint32_t)((row >> 1) & 3)) << 4) | (cb & 15u));
-                            asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr),
-                                         "r"(*reinterpret_cast<const uint32_t *>(&pr))
-                                         : "memory");
+                            asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(pk[e / 2]) : "memory");
                         }
                       } else {
                         // [channel][pixel] rows of 64 B: this lane's channel, 32 pixels.
@@ -631,7 +646,8 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(256, 4)
 to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S) {
     __shared__ __align__(16) T tile[kClC][kClS];
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    pdl_launch_dependents();   // the GEMM behind launches once every CTA here has started
+    pdl_wait();                // global memory only once the previous kernel is complete
     to_channels_last_block<T, VEC>(x, xc, C, Cp, S, blockIdx.x, blockIdx.y, blockIdx.z, tile);
 }
 
@@ -720,13 +736,6 @@ __device__ __forceinline__ void pack_tc_block(const T *__restrict__ w, T *__rest
         if (oc < OC && cp < Cp) wp[((int64_t)(t0 + tl) * OC + oc) * Cp + cp] = tile[o][cl][tl];
     }
 }
-template <typename T>
-__global__ void __launch_bounds__(256, 4)
-pack_tc_kernel(const T *__restrict__ w, T *__restrict__ wp, int OC, int C, int Cp, int taps, int ocpb) {
-    __shared__ T tile[kPkOc][kPkC][kPkT + 1];
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
-    pack_tc_block<T>(w, wp, OC, C, Cp, taps, ocpb, blockIdx.x, blockIdx.y, blockIdx.z, tile);
-}
 
 // CTA b of a grid that holds npk CTAs of one pass and nlay of another, the
 // pass with fewer CTAs first (measured: the other order leaves the smaller
@@ -756,7 +765,8 @@ prep_tc_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64
                const T *__restrict__ w, T *__restrict__ wp, int OC, int taps, int ocpb, int pkx, int pky, int npk,
                int nlay) {
     __shared__ __align__(16) unsigned char tile[prep_tile_bytes<T>()];
-    pdl_wait();   // dependents start when this grid completes
+    pdl_launch_dependents();   // the GEMM behind launches once every CTA here has started
+    pdl_wait();                // global memory only once the previous kernel is complete
     bool pack;
     const int q = prep_block_index(blockIdx.x, npk, nlay, &pack);
     if (pack)
@@ -765,6 +775,51 @@ prep_tc_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64
     else
         to_channels_last_block<T, VEC>(x, xc, C, Cp, S, q % clx, (q / clx) % cly, q / (clx * cly),
                                        reinterpret_cast<T (*)[kClS]>(tile));
+}
+
+// The weight pack for 16-bit data without shared memory: a grid of small
+// CTAs (128 threads, at most 80 registers each), one of which fits on an SM
+// next to a resident CTA of the tensor-core GEMM (the GEMM's shared memory
+// stays within 226 KB for this). The grid can therefore launch behind the
+// previous GEMM and wait at the dependency barrier on its SMs, and it lets
+// the next GEMM launch and set up while it works. An item is one output
+// channel oc, 64 channels and 8 taps: lane l takes channels 2l and 2l + 1,
+// issues all 16 loads of its 8 taps (2-byte elements, the run of taps of
+// each channel is contiguous in OIHW) before it stores, and writes
+// wp[tap][oc][c .. c+1] as one 32-bit word per tap, so a warp writes each
+// (tap, oc) row's 64 channels as 128 contiguous bytes; channels C .. Cp-1 are
+// zeros.
+constexpr int kPrThreads = 128;
+template <typename T>
+__global__ void __launch_bounds__(kPrThreads, 6)
+pack_rt_kernel(const unsigned short *__restrict__ w, unsigned int *__restrict__ wp, int OC, int C, int Cp, int taps,
+               long long items) {
+    static_assert(sizeof(T) == 2, "16-bit weights");
+    pdl_launch_dependents();   // the GEMM behind may launch and set up now
+    pdl_wait();                // wp only once the previous kernel (which may read it) is complete
+    const int lane = threadIdx.x & 31;
+    const long long nw = (long long)gridDim.x * (kPrThreads / 32);
+    const int pkb = (Cp + 63) / 64, pkt = (taps + 7) / 8;
+    for (long long q = (long long)(threadIdx.x >> 5) * gridDim.x + blockIdx.x; q < items; q += nw) {
+        const int oc = (int)(q / (pkb * pkt));
+        const int rem = (int)(q - (long long)oc * pkb * pkt);
+        const int c = (rem / pkt) * 64 + 2 * lane, t0 = (rem % pkt) * 8;
+        if (c >= Cp) continue;
+        const unsigned short *w0 = w + ((long long)oc * C + c) * taps;
+        uint32_t pr[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = t0 + k;
+            const uint32_t lo = (t < taps && c < C) ? (uint32_t)__ldg(w0 + t) : 0u;
+            const uint32_t hi = (t < taps && c + 1 < C) ? (uint32_t)__ldg(w0 + taps + t) : 0u;
+            pr[k] = lo | (hi << 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = t0 + k;
+            if (t < taps) wp[(((long long)t * OC + oc) * Cp + c) / 2] = pr[k];
+        }
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -841,7 +896,9 @@ int stages_for(const Problem &p, int np, bool single) {
     const int split = p.dtype == GBCONV_F32 ? 2 : 1;
     const int stage_bytes = split * ((int)kWStageBytes + np * 128);
     const int fixed = 1024 + (single ? 0 : (int)ystage_bytes(p)) + 256;
-    int st = (227 * 1024 - fixed) / stage_bytes;
+    // 226 KB at most, so that a CTA of the small layout / pack grid (no
+    // shared memory of its own) still fits on the SM next to this one
+    int st = (226 * 1024 - fixed) / stage_bytes;
     if (st > kMaxStages) st = kMaxStages;
     // the epilogue's staging reuses the ring of a single-tile CTA
     if (single && (int64_t)st * stage_bytes < (int64_t)ystage_bytes(p)) return 0;
@@ -1152,17 +1209,20 @@ template <bool VEC>
 __global__ void __launch_bounds__(256)
 split_nchw_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t S) {
     __shared__ float tile[kSpC][kSpS + 1];
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    pdl_launch_dependents();   // the GEMM behind launches once every CTA here has started
+    pdl_wait();                // global memory only once the previous kernel is complete
     split_nchw_block<VEC>(x, xs, C, Cs, S, blockIdx.x, blockIdx.y, blockIdx.z, tile);
 }
 __global__ void __launch_bounds__(256)
 split_cl_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, int Cs, int64_t positions) {
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    pdl_launch_dependents();   // the GEMM behind launches once every CTA here has started
+    pdl_wait();                // global memory only once the previous kernel is complete
     split_cl_elem(x, xs, C, Cs, positions, (int64_t)blockIdx.x * blockDim.x + threadIdx.x);
 }
 __global__ void __launch_bounds__(256)
 pack_split_kernel(const float *__restrict__ w, float *__restrict__ wp, int OC, int C, int Cs, int taps) {
-    pdl_wait();   // launched early behind a GEMM; dependents start when this grid completes
+    pdl_launch_dependents();   // the GEMM behind launches once every CTA here has started
+    pdl_wait();                // global memory only once the previous kernel is complete
     pack_split_elem(w, wp, OC, C, Cs, taps, (int64_t)blockIdx.x * blockDim.x + threadIdx.x);
 }
 // The split-pack of OIHW weights and the split of x as one grid: npk CTAs
@@ -1175,7 +1235,8 @@ prep_split_kernel(const float *__restrict__ x, float *__restrict__ xs, int C, in
                   int spx, int spy, const float *__restrict__ w, float *__restrict__ wp, int OC, int taps, int npk,
                   int nsp) {
     __shared__ float tile[kSpC][kSpS + 1];
-    pdl_wait();   // dependents start when this grid completes
+    pdl_launch_dependents();   // the GEMM behind launches once every CTA here has started
+    pdl_wait();                // global memory only once the previous kernel is complete
     bool pack;
     const int q = prep_block_index(blockIdx.x, npk, nsp, &pack);
     if (pack) {
@@ -1222,13 +1283,19 @@ cudaError_t launch_cl_typed(const Problem &p, const void *x, void *xc, cudaStrea
 
 template <typename T>
 cudaError_t launch_pack_tc_typed(const Problem &p, const void *w, void *wp, cudaStream_t s) {
+    DevInfo info;
+    cudaError_t e = dev_info(&info);
+    if (e != cudaSuccess) return e;
     const int Cp = tc_cpad(p.C);
-    const int ocpb = pack_oc_block(p.taps);
-    dim3 grid((unsigned)((p.OC + ocpb - 1) / ocpb), (unsigned)((Cp + kPkC - 1) / kPkC),
-              (unsigned)((p.taps + kPkT - 1) / kPkT));
-    return launch_pdl(pack_tc_kernel<T>, grid, dim3(256), 0, s, static_cast<const T *>(w), static_cast<T *>(wp),
-                      p.OC, p.C, Cp, p.taps, ocpb);
-    return cudaGetLastError();
+    const long long items = (long long)p.OC * ((Cp + 63) / 64) * ((p.taps + 7) / 8);
+    // four CTAs per SM, also when there are fewer items than warps (item q
+    // goes to CTA q % grid, so the items spread over all SMs): the CTA beside
+    // a resident GEMM CTA is joined by the others once that GEMM has left
+    const long long grid = 4ll * info.sms;
+    if (log_enabled()) log_line("pack_rt_kernel grid=%lld block=%d items=%lld", grid, kPrThreads, items);
+    return launch_pdl(pack_rt_kernel<T>, dim3((unsigned)grid), dim3(kPrThreads), 0, s,
+                      static_cast<const unsigned short *>(w), static_cast<unsigned int *>(wp), p.OC, p.C, Cp,
+                      p.taps, items);
 }
 
 template <typename T>
@@ -1310,7 +1377,6 @@ cudaError_t launch_pack_tc(const Problem &p, const void *w, void *wp, cudaStream
         const int64_t n = (int64_t)p.taps * p.OC * Cs;
         return launch_pdl(pack_split_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s,
                           static_cast<const float *>(w), static_cast<float *>(wp), p.OC, p.C, Cs, p.taps);
-        return cudaGetLastError();
     }
     if (p.dtype == GBCONV_BF16) return launch_pack_tc_typed<__nv_bfloat16>(p, w, wp, s);
     return launch_pack_tc_typed<__half>(p, w, wp, s);
