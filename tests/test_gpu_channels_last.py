@@ -71,6 +71,8 @@ SWEEP = [
     (A_TC, _L(dtype="bf16", C=16, H=20, W=70, OC=64, stride=2)),
     (A_TC, _L(C=8, H=7, W=12, OC=7, bias=False)),                  # odd OC: scalar stores
     (A_TC, _L(C=32, H=6, W=20, OC=136)),                           # two output-channel tiles
+    (A_TC, _L(N=3, C=64, H=30, W=40, OC=320)),                     # three channel tiles, more tiles than SMs
+    (A_TC, _L(dtype="bf16", C=24, H=7, W=9, OC=264, relu=True)),   # three channel tiles, an OC tail
     (A_TC, _L(N=2, C=24, H=16, W=10, OC=32, k=1, pad=0)),          # several rows per tile
     (A_TC, _L(C=16, H=3, W=300, OC=16, k=5, pad=2)),               # column tiles
     (A_TC, _L(C=72, H=5, W=9, OC=24, k=3, pad=0, stride=3)),       # ragged channel block

@@ -194,6 +194,14 @@ SWEEP = [
     (A_TC, _L(N=16, C=32, H=40, W=64, OC=32, relu=True)),
     (A_TC, _L(dtype="f16", N=16, C=64, H=40, W=64, OC=64)),
     (A_TC, _L(N=4, C=32, H=64, W=100, OC=32, bias=False)),
+    # 16-bit, more than 128 output channels (several output-channel tiles):
+    # more tiles than SMs (persistent loop, two accumulators), three full
+    # channel tiles over small images (tiles cross images), 3D with an OC
+    # tail, bf16 with stride 2
+    (A_TC, _L(dtype="f16", N=4, C=64, H=40, W=64, OC=256)),
+    (A_TC, _L(dtype="bf16", N=3, C=40, H=9, W=11, OC=384, relu=True)),
+    (A_TC, _L(dtype="f16", C=32, D=3, H=8, W=30, OC=260, ndim=3)),
+    (A_TC, _L(dtype="bf16", N=2, C=72, H=33, W=47, OC=200, stride=2, bias=False)),
     # more row tiles than CTAs with a partial last wave, 2D and 3D
     (A_TC, _L(dtype="f16", N=2, C=16, H=100, W=160, OC=32, relu=True)),
     (A_TC, _L(dtype="bf16", C=16, D=3, H=70, W=240, OC=16, ndim=3, tpad=CAUSAL)),
