@@ -50,7 +50,16 @@ WORKLOADS = {"detection_stem": 2, "tiny": 1, "text_line_batch": 3,
 VARIANTS = {"detection_stem_maxpool": (2, {"pool": True}, "+maxpool2x2"),
             "video_vae_conv3d_f16_causal": (5, {"tpad": 1}, "+causal_frames"),
             "wide_dense_f16_channels_last": (4, {"cl": True}, "+channels_last"),
-            "video_vae_conv3d_f16_channels_last": (5, {"cl": True}, "+channels_last")}
+            "video_vae_conv3d_f16_channels_last": (5, {"cl": True}, "+channels_last"),
+            "text_line_batch_exact_fp32": (3, {}, "+exact_fp32_cuda_cores")}
+# Variants that force an algorithm: the fp32 layer on the CUDA cores (exact
+# fp32 FMAs) instead of the tensor cores' three TF32 products.
+VARIANT_ALGO = {"text_line_batch_exact_fp32": "IGEMM_FFMA"}
+
+
+def workload_algo(gb, name):
+    """The algorithm a workload forces (ALGO_AUTO unless it names one)."""
+    return getattr(gb, "ALGO_" + VARIANT_ALGO[name]) if name in VARIANT_ALGO else gb.ALGO_AUTO
 
 
 def workload_layer(name):
@@ -300,7 +309,8 @@ def run_ours(args):
     inp = synthetic.make_inputs(L)
     x, w = to_device(device_x(L, inp), L.dtype, dev), to_device(inp.w, L.dtype, dev)
     b = torch.from_numpy(inp.b).to(dev)
-    conv = Conv(x, w, b, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool, channels_last=L.cl)
+    algo = workload_algo(gb, args.workload)
+    conv = Conv(x, w, b, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool, channels_last=L.cl, algo=algo)
     # the tensor-core GEMM's x layout pass (when x is not read in place)
     # shares one launch with the weight pack
     launches = {gb.ALGO_DIRECT: 1, gb.ALGO_DIRECT_TC: 1, gb.ALGO_IGEMM_FFMA: 2,
@@ -337,8 +347,9 @@ def run_ours(args):
         kernel, kfile = {gb.ALGO_DIRECT: ("direct_stem_kernel", "direct_stem.cu") if stem
                          else ("direct_conv_kernel", "direct.cu"),
                          gb.ALGO_DIRECT_TC: ("stem_tf32_kernel", "stem_tf32.cuh"),
-                         gb.ALGO_IGEMM_FFMA: ("igemm_ffma2_kernel" if L.C % 16 == 0 else "igemm_ffma_kernel",
-                                              "igemm_ffma.cu"),
+                         gb.ALGO_IGEMM_FFMA: (("igemm_ffma_kernel" if L.C % 16 or L.cl else
+                                               "igemm_ffma_cp_kernel" if L.dtype == "f32" else
+                                               "igemm_ffma2_kernel"), "igemm_ffma.cu"),
                          gb.ALGO_IGEMM_TC: ("igemm_tc_kernel", "igemm_tc.cu")}[conv.algo]
         kernel_key = f"{kernel}:{L.name}"
         if conv.algo in (gb.ALGO_DIRECT, gb.ALGO_DIRECT_TC):
@@ -425,7 +436,8 @@ def run_ours(args):
             xj.copy_(x)
             wj.copy_(w)
             bj.copy_(b)
-            cj = Conv(xj, wj, bj, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool, channels_last=L.cl)
+            cj = Conv(xj, wj, bj, L.stride, L.pad, L.relu, tpad=L.tpad, pool=L.pool, channels_last=L.cl,
+                      algo=algo)
             hyj = torch.empty(cj.y.shape, dtype=cj.y.dtype).pin_memory()
             pipes.append((torch.cuda.Stream(), xj, wj, bj, cj, hyj))
         torch.cuda.synchronize()
@@ -505,9 +517,9 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
     back-to-back time with L2-resident buffers."""
     out = []
     p32 = fp32_peak_tflops(pk, sms)
-    layers = sorted(synthetic.LAYERS.items()) + [
-        (VARIANTS[v][0], workload_layer(v)) for v in sorted(VARIANTS)]
-    for idx, L in layers:
+    layers = [(idx, L, gb.ALGO_AUTO) for idx, L in sorted(synthetic.LAYERS.items())] + [
+        (VARIANTS[v][0], workload_layer(v), workload_algo(gb, v)) for v in sorted(VARIANTS)]
+    for idx, L, algo in layers:
         inp = synthetic.make_inputs(L)
         x, w = to_device(device_x(L, inp), L.dtype, dev), to_device(inp.w, L.dtype, dev)
         b = torch.from_numpy(inp.b).to(dev)
@@ -520,7 +532,7 @@ def per_layer(gb, Conv, to_device, torch, dev, timed_calls, pk, sms):
         t_ideal = max(t_c, t_m)
         for prepack in (False, True):
             conv = Conv(x, w, b, L.stride, L.pad, L.relu, prepack=prepack, tpad=L.tpad, pool=L.pool,
-                        channels_last=L.cl)
+                        channels_last=L.cl, algo=algo)
             rot = Rotation(torch, conv)
             calls = 200 if idx <= 3 else (100 if idx == 4 else 40)
             for _ in range(3):

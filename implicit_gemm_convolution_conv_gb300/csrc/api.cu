@@ -233,7 +233,8 @@ gbconv_status forward(const gbconv_desc *d, int ndim, const void *x,
             e = launch_pack_ffma(p, w, wsp + ws.w_off, s);
             wp = wsp + ws.w_off;
         }
-        if (e == cudaSuccess) e = launch_igemm_ffma(p, x, wp, b, y, s);
+        float *part = ws.part_bytes ? reinterpret_cast<float *>(wsp + ws.part_off) : nullptr;
+        if (e == cudaSuccess) e = launch_igemm_ffma(p, x, wp, b, y, part, ffma_split_slices(p), s);
         break;
     }
     case GBCONV_ALGO_IGEMM_TC: {
@@ -288,6 +289,11 @@ Workspace workspace_layout(const Problem &p) {
         ws.w_off = off;
         ws.w_bytes = packed_weight_bytes(p);
         off = align256(off + ws.w_bytes);
+    }
+    if (p.algo == GBCONV_ALGO_IGEMM_FFMA && ffma_split_slices(p) > 0) {
+        ws.part_off = off;
+        ws.part_bytes = (size_t)ffma_split_slices(p) * p.OC * p.N * p.out_vol * sizeof(float);
+        off = align256(off + ws.part_bytes);
     }
     ws.total = off;
     return ws;

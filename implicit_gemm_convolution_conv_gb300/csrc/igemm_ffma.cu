@@ -39,6 +39,11 @@ struct FfmaArgs {
     // pixel * ys_p, pixel = (od * OH + oh) * OW + ow.
     int64_t xs_n, xs_c, xs_d, xs_h, xs_w;
     int64_t ys_n, ys_c, ys_p;
+    // split-K (fp32 cp.async kernel): CTA z of gridDim.z sums K steps
+    // [ksteps z / splits, ksteps (z + 1) / splits) and stores the raw sums to
+    // part[z][oc][m]; null: the CTA covers all of K and applies the epilogue.
+    float *part;
+    int splits;
 };
 
 template <typename T>
@@ -289,11 +294,206 @@ __global__ void __launch_bounds__(WNT, kWideMinBlocks) igemm_ffma2_kernel(const 
     }
 }
 
+// fp32 variant of the packed-FMA kernel (channel counts that are multiples
+// of 16, NC(D)HW): the operand tiles go straight from global to shared
+// memory with cp.async, four stages deep, so no thread stages them through
+// registers and a thread needs at most 128 registers (several CTAs per SM).
+// CTA tile 128 pixels x BN channels (BN 128 or 64), 2 * BN threads; a
+// thread owns pixels 4 tm .. 4 tm + 3 and 64 + 4 tm .. + 3 (tm = tid % 16)
+// and channels 4 tn .. 4 tn + 3 and BN / 2 + 4 tn .. + 3 (tn = tid / 16),
+// accumulated as pixel pairs x channel with fma.rn.f32x2 (each weight is
+// duplicated into a register pair). The A tile is [16 k][128 pixels]: each
+// element is one 4-byte copy from x at the pixel's tap-shifted position,
+// zero-filled at padding and past the last pixel (cp.async with a source
+// size of 0); the B tile is [16 k][BN] straight from the packed weights
+// [K][OCp] in 16-byte copies. (Copying each A element twice, so that the
+// duplicated operand is A's and comes from shared memory, measured slower:
+// the doubled A tile leaves fewer CTAs per SM.)
+constexpr int CBM = 128, CBK = 16, CSTAGES = 4;
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool ok) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int BN>
+__global__ void __launch_bounds__(2 * BN, BN == 128 ? 2 : 3) igemm_ffma_cp_kernel(const FfmaArgs a) {
+    constexpr int NT = 2 * BN;
+    constexpr int A_PER = CBK * CBM / NT;          // A elements a thread copies per stage
+    constexpr int B_PER = CBK * BN / 4 / NT;        // 16-byte B chunks a thread copies per stage
+    constexpr int STAGE_A = CBK * CBM, STAGE_B = CBK * BN;   // floats
+    extern __shared__ __align__(16) float smem_f[];
+    float *As = smem_f;                              // [CSTAGES][CBK][CBM]
+    float *Bs = smem_f + CSTAGES * STAGE_A;          // [CSTAGES][CBK][BN]
+    const uint32_t As_s = static_cast<uint32_t>(__cvta_generic_to_shared(As));
+    const uint32_t Bs_s = static_cast<uint32_t>(__cvta_generic_to_shared(Bs));
+    // programmatic dependent launch: the next kernel launches once every CTA
+    // here has started; global memory only after the previous kernel is done
+    pdl_launch_dependents();
+    pdl_wait();
+
+    const float *x = static_cast<const float *>(a.x);
+    const float *wp = static_cast<const float *>(a.wp);
+    const int tid = threadIdx.x;
+    const int64_t m0 = (int64_t)blockIdx.x * CBM;
+    const int n0 = blockIdx.y * BN;
+
+    // A copier: pixel column tid % 128, k rows tid / 128 + (NT / 128) j.
+    const int a_col = tid % CBM, a_row0 = tid / CBM;
+    constexpr int A_ROW_STEP = NT / CBM;
+    const int64_t my_m = m0 + a_col;
+    const bool m_ok = my_m < a.M;
+    int img = 0, od = 0, oh = 0, ow = 0;
+    if (m_ok) {
+        int64_t r = my_m;
+        img = (int)(r / a.out_vol); r -= (int64_t)img * a.out_vol;
+        od = (int)(r / ((int64_t)a.OH * a.OW)); r -= (int64_t)od * a.OH * a.OW;
+        oh = (int)(r / a.OW); ow = (int)(r - (int64_t)oh * a.OW);
+    }
+    const int id0 = od * a.stride - a.pad_d, ih0 = oh * a.stride - a.pad, iw0 = ow * a.stride - a.pad;
+    const int64_t c_stride = (int64_t)a.D * a.in_hw;
+    const float *x_img = x + (int64_t)img * a.C * c_stride;
+
+    auto load_stage = [&](int ks, int buf) {
+        const int k0 = ks * CBK;
+        const int tap = k0 / a.C, c0 = k0 - tap * a.C;
+        const int kx = tap % a.k, ky = (tap / a.k) % a.k, kz = tap / (a.k * a.k);
+        const int id = id0 + kz, ih = ih0 + ky, iw = iw0 + kx;
+        const bool ok = m_ok && id >= 0 && id < a.D && ih >= 0 && ih < a.H && iw >= 0 && iw < a.W;
+        // a padding element reads nothing (source size 0); its address stays inside x
+        const float *src = ok ? x_img + (int64_t)(c0 + a_row0) * c_stride + (int64_t)id * a.in_hw +
+                                    (int64_t)ih * a.W + iw
+                              : x;
+        const int64_t step = ok ? (int64_t)A_ROW_STEP * c_stride : 0;
+        const uint32_t adst = As_s + (uint32_t)(buf * STAGE_A + a_row0 * CBM + a_col) * 4u;
+#pragma unroll
+        for (int j = 0; j < A_PER; ++j)
+            cp_async4(adst + (uint32_t)(j * A_ROW_STEP * CBM) * 4u, src + j * step, ok);
+        const uint32_t bdst = Bs_s + (uint32_t)(buf * STAGE_B) * 4u;
+#pragma unroll
+        for (int j = 0; j < B_PER; ++j) {
+            const int q = tid + NT * j;                 // chunk: row q / (BN / 4), 4 channels
+            const int row = q / (BN / 4), c4 = q % (BN / 4);
+            cp_async16(bdst + (uint32_t)(row * BN + 4 * c4) * 4u, wp + (int64_t)(k0 + row) * a.OCp + n0 + 4 * c4);
+        }
+    };
+
+    const int tm = tid % 16, tn = tid / 16;
+    float2 acc[4][8];   // [pixel pair][channel]
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+
+    const int ksteps_all = a.K / CBK;
+    const int z = blockIdx.z;
+    const int ks_first = a.part ? (int)((int64_t)ksteps_all * z / a.splits) : 0;
+    const int ksteps = a.part ? (int)((int64_t)ksteps_all * (z + 1) / a.splits) - ks_first : ksteps_all;
+#pragma unroll
+    for (int st = 0; st < CSTAGES - 1; ++st) {
+        if (st < ksteps) load_stage(ks_first + st, st);
+        cp_async_commit();
+    }
+    for (int ks = 0; ks < ksteps; ++ks) {
+        // stage ks has landed (for every thread's copies after the barrier),
+        // and every thread is done with the buffer the next load overwrites
+        cp_async_wait<CSTAGES - 2>();
+        __syncthreads();
+        if (ks + CSTAGES - 1 < ksteps) load_stage(ks_first + ks + CSTAGES - 1, (ks + CSTAGES - 1) % CSTAGES);
+        cp_async_commit();
+        const float *Ab = As + (ks % CSTAGES) * STAGE_A;
+        const float *Bb = Bs + (ks % CSTAGES) * STAGE_B;
+#pragma unroll
+        for (int kk = 0; kk < CBK; ++kk) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&Ab[kk * CBM + 4 * tm]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&Ab[kk * CBM + 64 + 4 * tm]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&Bb[kk * BN + 4 * tn]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&Bb[kk * BN + BN / 2 + 4 * tn]);
+            const float2 av[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
+                                  make_float2(a1.z, a1.w)};
+            const float bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float2 bv = make_float2(bw[j], bw[j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i][j] = __ffma2_rn(av[i], bv, acc[i][j]);
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    if (a.part) {
+        // raw partial sums, part[z][oc][m]: runs of 4 pixels as vectors
+        // when M % 4 == 0 (the run then lies whole inside M)
+        float *pz = a.part + (int64_t)z * a.OC * a.M;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int64_t m = m0 + 64 * r + 4 * tm;
+            if (m >= a.M) continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int oc = n0 + (j < 4 ? 4 * tn + j : BN / 2 + 4 * tn + j - 4);
+                if (oc >= a.OC) continue;
+                float *dst = pz + (int64_t)oc * a.M + m;
+                const float v[4] = {acc[2 * r][j].x, acc[2 * r][j].y, acc[2 * r + 1][j].x, acc[2 * r + 1][j].y};
+                if ((a.M & 3) == 0) {
+                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (m + e < a.M) dst[e] = v[e];
+                }
+            }
+        }
+        return;
+    }
+
+    // Epilogue: for each channel, the thread's two runs of 4 pixels; a run
+    // inside one image's plane with y 16-byte aligned leaves as one vector.
+    float *y = static_cast<float *>(a.y);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int64_t m = m0 + 64 * r + 4 * tm;
+        if (m >= a.M) continue;
+        const int64_t im = m / a.out_vol, pix = m - im * a.out_vol;
+        const bool vec = pix + 4 <= a.out_vol && m + 4 <= a.M && ((a.out_vol | pix) & 3) == 0 &&
+                         ((uintptr_t)y & 15) == 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int oc = n0 + (j < 4 ? 4 * tn + j : BN / 2 + 4 * tn + j - 4);
+            if (oc >= a.OC) continue;
+            const float bias = a.b ? __ldg(a.b + oc) : 0.0f;
+            const float v[4] = {acc[2 * r][j].x, acc[2 * r][j].y, acc[2 * r + 1][j].x, acc[2 * r + 1][j].y};
+            if (vec) {
+                *reinterpret_cast<float4 *>(y + (im * a.OC + oc) * a.out_vol + pix) =
+                    make_float4(epilogue(v[0], bias, a.relu), epilogue(v[1], bias, a.relu),
+                                epilogue(v[2], bias, a.relu), epilogue(v[3], bias, a.relu));
+            } else {
+                int64_t n = im, pp = pix;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (m + e < a.M) y[(n * a.OC + oc) * a.out_vol + pp] = epilogue(v[e], bias, a.relu);
+                    if (++pp == a.out_vol) { pp = 0; ++n; }
+                }
+            }
+        }
+    }
+}
+
 // wp[(tap * C + c) * OCp + oc] = w[(oc * C + c) * taps + tap], zero-padded in
 // oc. One CTA per (tap, c) row of the output; threads walk the channels.
 template <typename T>
 __global__ void pack_ffma_kernel(const T *__restrict__ w, T *__restrict__ wp,
                                  int OC, int C, int taps, int OCp) {
+    pdl_launch_dependents();
+    pdl_wait();   // wp may still be read by the previous call's GEMM
     const int row = blockIdx.x;                 // tap * C + c
     const int tap = row / C, c = row - tap * C;
     const T *src = w + (int64_t)c * taps + tap;
@@ -302,8 +502,101 @@ __global__ void pack_ffma_kernel(const T *__restrict__ w, T *__restrict__ wp,
         dst[oc] = oc < OC ? src[(int64_t)oc * C * taps] : T(0.0f);
 }
 
+// Split-K reduction: y = epilogue(sum over z of part[z][oc][m]), the
+// slices added in order z = 0, 1, ... (the same result on every call). A
+// thread takes 4 consecutive pixels of one channel.
+__global__ void __launch_bounds__(256) ffma_split_reduce_kernel(const FfmaArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t mq = (a.M + 3) / 4;
+    const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (q >= mq * a.OC) return;
+    const int oc = (int)(q / mq);
+    const int64_t m = (q - (int64_t)oc * mq) * 4;
+    const bool whole = (a.M & 3) == 0;
+    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int z = 0; z < a.splits; ++z) {
+        const float *src = a.part + ((int64_t)z * a.OC + oc) * a.M + m;
+        if (whole) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
+            v[0] += t.x; v[1] += t.y; v[2] += t.z; v[3] += t.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (m + e < a.M) v[e] += __ldg(src + e);
+        }
+    }
+    const float bias = a.b ? __ldg(a.b + oc) : 0.0f;
+    float *y = static_cast<float *>(a.y);
+    const int64_t im = m / a.out_vol, pix = m - im * a.out_vol;
+    if (m + 4 <= a.M && pix + 4 <= a.out_vol && ((a.out_vol | pix) & 3) == 0 && ((uintptr_t)y & 15) == 0) {
+        *reinterpret_cast<float4 *>(y + (im * a.OC + oc) * a.out_vol + pix) =
+            make_float4(epilogue(v[0], bias, a.relu), epilogue(v[1], bias, a.relu), epilogue(v[2], bias, a.relu),
+                        epilogue(v[3], bias, a.relu));
+    } else {
+        int64_t n = im, pp = pix;
+        for (int e = 0; e < 4 && m + e < a.M; ++e) {
+            y[(n * a.OC + oc) * a.out_vol + pp] = epilogue(v[e], bias, a.relu);
+            if (++pp == a.out_vol) { pp = 0; ++n; }
+        }
+    }
+}
+
+// fp32 cp.async kernel. With fewer 128 x 128 tiles than SMs and room for
+// partial sums (slices > 1), K is split into S parts, S chosen to minimise
+// the parts the busiest SM runs (ceil(tiles S / SMs) / S of a tile: for 120
+// tiles on 152 SMs, S = 5 gives 0.8 against 1.0), then one reduction pass.
+// Without a split: 128 x 128 tiles, or 128 x 64 when even those fill at
+// most one wave (more, smaller CTAs).
+cudaError_t launch_ffma_cp(FfmaArgs a, float *part, int slices, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int64_t mt = (a.M + CBM - 1) / CBM;
+    const int64_t tiles = mt * ((a.OC + 127) / 128);
+    int split = 1;
+    if (part && slices > 1 && tiles < sms) {
+        double best = 1.0;
+        for (int S = 2; S <= slices; ++S) {
+            const double c = (double)((tiles * S + sms - 1) / sms) / S;
+            if (c < best - 1e-9) {
+                best = c;
+                split = S;
+            }
+        }
+        if (best > 0.9) split = 1;   // less than a tenth saved: not worth the reduction pass
+    }
+    a.part = split > 1 ? part : nullptr;
+    a.splits = split;
+    const bool wide = split > 1 || tiles * 2 > sms;
+    const int bn = wide ? 128 : 64;
+    const int smem = CSTAGES * (CBK * CBM + CBK * bn) * (int)sizeof(float);
+    dim3 grid((unsigned)mt, (unsigned)((a.OC + bn - 1) / bn), (unsigned)split);
+    if (log_enabled())
+        log_line("igemm_ffma_cp_kernel grid=%ux%ux%u block=%d smem=%d tile=%dx%d stages=%d%s", grid.x, grid.y, grid.z,
+                 2 * bn, smem, CBM, bn, CSTAGES, split > 1 ? " split_k (then ffma_split_reduce_kernel)" : "");
+    if (wide) {
+        e = cudaFuncSetAttribute(igemm_ffma_cp_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(igemm_ffma_cp_kernel<128>, grid, dim3(256), smem, s, a);
+    } else {
+        e = cudaFuncSetAttribute(igemm_ffma_cp_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(igemm_ffma_cp_kernel<64>, grid, dim3(128), smem, s, a);
+    }
+    if (e != cudaSuccess || split == 1) return e;
+    const int64_t n = (a.M + 3) / 4 * a.OC;
+    return launch_pdl(ffma_split_reduce_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, a);
+}
+
 template <typename T>
-cudaError_t launch_ffma_typed(const FfmaArgs &a, bool cl, cudaStream_t s) {
+cudaError_t launch_ffma_typed(const FfmaArgs &a, bool cl, float *part, int slices, cudaStream_t s) {
+    if constexpr (sizeof(T) == 4) {
+        // 16-byte weight copies and 4-byte x copies need those alignments
+        if (a.C % CBK == 0 && !cl && (uintptr_t)a.wp % 16 == 0 && (uintptr_t)a.x % 4 == 0)
+            return launch_ffma_cp(a, part, slices, s);
+    }
     if (a.C % WBK == 0 && !cl) {
         auto kern = igemm_ffma2_kernel<T>;
         const int smem = (2 * 2 * WBK * WBM + 2 * WBK * WBN) * (int)sizeof(float);
@@ -326,15 +619,27 @@ cudaError_t launch_ffma_typed(const FfmaArgs &a, bool cl, cudaStream_t s) {
 template <typename T>
 cudaError_t launch_pack_typed(const Problem &p, const void *w, void *wp, cudaStream_t s) {
     const int OCp = ffma_ocpad(p.OC);
-    pack_ffma_kernel<T><<<p.taps * p.C, OCp < 256 ? OCp : 256, 0, s>>>(
-        static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.C, p.taps, OCp);
-    return cudaGetLastError();
+    return launch_pdl(pack_ffma_kernel<T>, dim3((unsigned)(p.taps * p.C)), dim3(OCp < 256 ? OCp : 256), 0, s,
+                      static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.C, p.taps, OCp);
 }
 
 }  // namespace
 
+int ffma_split_slices(const Problem &p) {
+    if (p.dtype != GBCONV_F32 || p.cl || p.C % CBK != 0) return 0;
+    const int64_t M = (int64_t)p.N * p.out_vol;
+    // Layers with at least 160 tiles of 128 x 128 already fill the SMs (152
+    // on a GB300) and get no split, nor the room for one.
+    if ((M + 127) / 128 * ((p.OC + 127) / 128) >= 160) return 0;
+    const int ksteps = p.taps * p.C / CBK;
+    int slices = ksteps / 2 < 8 ? ksteps / 2 : 8;
+    const int64_t slice_bytes = (int64_t)p.OC * M * (int64_t)sizeof(float);
+    while (slices > 1 && slices * slice_bytes > (64ll << 20)) --slices;
+    return slices >= 2 ? slices : 0;
+}
+
 cudaError_t launch_igemm_ffma(const Problem &p, const void *x, const void *wp,
-                              const float *b, void *y, cudaStream_t s) {
+                              const float *b, void *y, float *part, int slices, cudaStream_t s) {
     FfmaArgs a{};
     a.x = x; a.wp = wp; a.b = b; a.y = y;
     a.C = p.C; a.D = p.D; a.H = p.H; a.W = p.W; a.OC = p.OC; a.OCp = ffma_ocpad(p.OC);
@@ -355,9 +660,9 @@ cudaError_t launch_igemm_ffma(const Problem &p, const void *x, const void *wp,
         a.ys_c = p.out_vol; a.ys_p = 1;
     }
     switch (p.dtype) {
-    case GBCONV_F32: return launch_ffma_typed<float>(a, p.cl, s);
-    case GBCONV_F16: return launch_ffma_typed<__half>(a, p.cl, s);
-    default: return launch_ffma_typed<__nv_bfloat16>(a, p.cl, s);
+    case GBCONV_F32: return launch_ffma_typed<float>(a, p.cl, part, slices, s);
+    case GBCONV_F16: return launch_ffma_typed<__half>(a, p.cl, nullptr, 0, s);
+    default: return launch_ffma_typed<__nv_bfloat16>(a, p.cl, nullptr, 0, s);
     }
 }
 

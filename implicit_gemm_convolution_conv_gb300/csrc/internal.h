@@ -54,8 +54,13 @@ size_t packed_weight_bytes(const Problem &p);
 struct Workspace {
     size_t x_off = 0, x_bytes = 0;   // channels-last x (tensor-core path)
     size_t w_off = 0, w_bytes = 0;   // packed weights (when w_layout == OIHW)
+    size_t part_off = 0, part_bytes = 0;   // split-K partial sums (fp32 CUDA-core GEMM)
     size_t total = 0;
 };
+// fp32 CUDA-core GEMM split over K (few tiles for the SMs): the partial-sum
+// slices the workspace holds for it ([splits][OC][M] fp32), 0 when the layer
+// does not qualify.
+int ffma_split_slices(const Problem &p);
 Workspace workspace_layout(const Problem &p);
 
 // Whether a kernel family can run a problem (shared-memory and box limits).
@@ -69,9 +74,11 @@ cudaError_t launch_direct(const Problem &p, const void *x, const void *w_oihw,
                           const float *b, void *y, cudaStream_t s);
 cudaError_t launch_direct_stem(const Problem &p, const void *x, const void *w_oihw,
                                const float *b, void *y, cudaStream_t s);
+// part: room for `slices` fp32 partial-sum slices of [OC][M] (split-K), or
+// null (no split).
 cudaError_t launch_igemm_ffma(const Problem &p, const void *x,
                               const void *w_packed, const float *b, void *y,
-                              cudaStream_t s);
+                              float *part, int slices, cudaStream_t s);
 cudaError_t launch_pack_ffma(const Problem &p, const void *w_oihw,
                              void *w_packed, cudaStream_t s);
 cudaError_t launch_pack_tc(const Problem &p, const void *w_oihw,

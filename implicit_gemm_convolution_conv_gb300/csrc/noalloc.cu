@@ -112,6 +112,7 @@ extern "C" gbconv_status gbconv_conv_fwd_noalloc(const gbconv_desc *desc, int nd
     }
     if (overlap(y, yb, scratch, wp_bytes)) return GBCONV_ERR_OVERLAP;
     cudaError_t e = launch_pack_ffma(p, w, scratch, stream);
-    if (e == cudaSuccess) e = launch_igemm_ffma(p, x, scratch, b, y, stream);
+    // no workspace: no split-K partial sums either
+    if (e == cudaSuccess) e = launch_igemm_ffma(p, x, scratch, b, y, nullptr, 0, stream);
     return launch_status(e);   // the same mapping as the regular forward call
 }

@@ -148,6 +148,13 @@ SWEEP = [
     (A_FFMA, _L(C=6, D=5, H=6, W=7, OC=12, ndim=3)),
     (A_FFMA, _L(C=3, D=6, H=7, W=5, OC=65, ndim=3, stride=2, pad=2)),
     (A_FFMA, _L(dtype="f16", N=2, C=16, H=11, W=12, OC=40)),
+    # fp32 with C % 16 == 0 (cp.async stages): a ragged last pixel tile and
+    # an OC tail, 3D with stride 2, k = 5, and enough pixels for 128-channel
+    # tiles (more tiles than SMs)
+    (A_FFMA, _L(N=3, C=32, H=7, W=13, OC=70, relu=True)),
+    (A_FFMA, _L(C=16, D=4, H=6, W=10, OC=24, ndim=3, stride=2)),
+    (A_FFMA, _L(N=2, C=48, H=20, W=36, OC=200, k=5, pad=2, bias=False)),
+    (A_FFMA, _L(N=8, C=32, H=40, W=64, OC=130)),
     (A_FFMA, _L(dtype="bf16", C=12, H=9, W=9, OC=17, relu=True)),
     # tensor-core implicit GEMM: several tiles, ragged tails, partial
     # channel blocks, OC tails, strides, k 1/3/5, 3D incl. a single frame
