@@ -198,7 +198,11 @@ gbconv_status gbconv_output_shape(const gbconv_desc *desc, int ndim, int *OD,
  * Bytes of caller workspace the forward call needs for this desc (0 when the
  * chosen kernel needs none). Scratch holds the re-laid-out input (tensor-core
  * path: channels-last copy of x; for float32, x split into TF32 hi and lo
- * halves) and, with w_layout OIHW, the packed weights. Host only.
+ * halves), with w_layout OIHW the packed weights, and, for a float32 layer on
+ * the CUDA-core implicit GEMM (C a multiple of 16, NC(D)HW x) with fewer
+ * than 160 tiles of 128 pixels x 128 output channels, the fp32 partial sums
+ * of its split over K (at most 8 slices of OC x N x OD x OH x OW, 64 MB at
+ * most). Host only.
  */
 gbconv_status gbconv_workspace_size(const gbconv_desc *desc, int ndim,
                                     size_t *bytes);
