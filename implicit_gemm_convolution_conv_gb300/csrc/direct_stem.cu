@@ -397,8 +397,64 @@ cudaError_t launch_stem_cs(const Problem &p, const StemArgs &a, cudaStream_t s) 
     return p.pool ? launch_stem_csp<T, C, S, PAD, true>(p, a, s) : launch_stem_csp<T, C, S, PAD, false>(p, a, s);
 }
 
+// Layers this small (at most 65,536 outputs, no pool) are bound by the
+// dependent launch and one memory round trip, not by bandwidth or the FMA
+// pipes: one thread per output element issues all of its loads at once (the
+// C x 9 input values of its window, zero outside the input, and its C x 9
+// weights), then the FMAs and one store, with no halo ring to fill first.
+// The output index is NCHW order (ow fastest), so a warp's stores are
+// consecutive pixels of one channel plane.
+constexpr long long kTinyOutputs = 1 << 16;
+template <typename T, int C, int S>
+__global__ void __launch_bounds__(128) direct_tiny_kernel(const StemArgs a) {
+    pdl_launch_dependents();
+    // The output coordinates (32-bit: at most 65,536 outputs) before the
+    // dependency wait, which only global memory has to follow.
+    const unsigned total = (unsigned)a.N * a.OC * a.OH * a.OW;
+    const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned ow = i % (unsigned)a.OW;
+    unsigned r = i / (unsigned)a.OW;
+    const unsigned oh = r % (unsigned)a.OH;
+    r /= (unsigned)a.OH;
+    const unsigned oc = r % (unsigned)a.OC;
+    const unsigned n = r / (unsigned)a.OC;
+    const T *x = static_cast<const T *>(a.x) + (size_t)n * C * a.H * a.W;
+    const T *w = static_cast<const T *>(a.w) + (size_t)oc * C * 9;
+    pdl_wait();
+    if (i >= total) return;
+    float xv[C * 9], wv[C * 9];
+#pragma unroll
+    for (int c = 0; c < C; ++c)
+#pragma unroll
+        for (int ky = 0; ky < 3; ++ky)
+#pragma unroll
+            for (int kx = 0; kx < 3; ++kx) {
+                const int t = (c * 3 + ky) * 3 + kx;
+                const int ih = (int)oh * S - a.pad + ky, iw = (int)ow * S - a.pad + kx;
+                xv[t] = (ih >= 0 && ih < a.H && iw >= 0 && iw < a.W)
+                            ? Storage<T>::load(x + ((size_t)c * a.H + ih) * a.W + iw)
+                            : 0.0f;
+                wv[t] = Storage<T>::load(w + t);
+            }
+    const float bias = a.b ? __ldg(a.b + oc) : 0.0f;
+    float acc = 0.0f;
+#pragma unroll
+    for (int t = 0; t < C * 9; ++t) acc = fmaf(xv[t], wv[t], acc);
+    static_cast<T *>(a.y)[i] = Storage<T>::from_float(epilogue(acc, bias, a.relu));
+}
+
+template <typename T, int C>
+cudaError_t launch_tiny_c(const Problem &p, const StemArgs &a, cudaStream_t s) {
+    const long long total = (long long)p.N * p.OC * p.OH * p.OW;
+    const dim3 grid((unsigned)((total + 127) / 128));
+    if (log_enabled()) log_line("direct_tiny_kernel grid=%u block=128 outputs=%lld", grid.x, total);
+    if (p.stride == 1) return launch_pdl(direct_tiny_kernel<T, C, 1>, grid, dim3(128), 0, s, a);
+    return launch_pdl(direct_tiny_kernel<T, C, 2>, grid, dim3(128), 0, s, a);
+}
+
 template <typename T, int C>
 cudaError_t launch_stem_c(const Problem &p, const StemArgs &a, cudaStream_t s) {
+    if (!p.pool && (long long)p.N * p.OC * p.OH * p.OW <= kTinyOutputs) return launch_tiny_c<T, C>(p, a, s);
     if (p.pad == 0)
         return p.stride == 1 ? launch_stem_cs<T, C, 1, 0>(p, a, s) : launch_stem_cs<T, C, 2, 0>(p, a, s);
     return p.stride == 1 ? launch_stem_cs<T, C, 1, 1>(p, a, s) : launch_stem_cs<T, C, 2, 1>(p, a, s);

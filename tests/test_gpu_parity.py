@@ -140,6 +140,11 @@ SWEEP = [
     (A_DIRECT, _L(C=4, H=18, W=36, OC=64, stride=2, pad=0, relu=True)),
     (A_DIRECT, _L(C=1, N=2, H=7, W=44, OC=36, stride=1)),
     (A_DIRECT, _L(dtype="f16", C=3, H=24, W=64, OC=16, stride=2)),
+    # more than 65,536 outputs: the stem kernel's halo ring (smaller layers
+    # take one thread per output): stride 2, two channel blocks, bf16
+    (A_DIRECT, _L(dtype="f16", C=3, H=130, W=200, OC=32, stride=2)),
+    (A_DIRECT, _L(C=1, N=2, H=70, W=130, OC=36)),
+    (A_DIRECT, _L(dtype="bf16", C=3, H=90, W=100, OC=8, relu=True)),
     # CUDA-core implicit GEMM: ragged M, N and K, strides, 3D
     (A_FFMA, _L(N=2, C=20, H=9, W=13, OC=130, relu=True)),
     (A_FFMA, _L(C=64, H=12, W=80, OC=128)),
