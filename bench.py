@@ -344,8 +344,10 @@ def run_ours(args):
     line = None
     if rank == 0:
         stem = L.ndim == 2 and L.C <= 4 and L.k == 3 and L.stride in (1, 2)
-        kernel, kfile = {gb.ALGO_DIRECT: ("direct_stem_kernel", "direct_stem.cu") if stem
-                         else ("direct_conv_kernel", "direct.cu"),
+        # stems of at most 65,536 outputs (no pool) run one thread per output
+        tiny = stem and not L.pool and int(np.prod(L.y_shape())) <= 1 << 16
+        kernel, kfile = {gb.ALGO_DIRECT: (("direct_tiny_kernel" if tiny else "direct_stem_kernel"), "direct_stem.cu")
+                         if stem else ("direct_conv_kernel", "direct.cu"),
                          gb.ALGO_DIRECT_TC: ("stem_tf32_kernel", "stem_tf32.cuh"),
                          gb.ALGO_IGEMM_FFMA: (("igemm_ffma_kernel" if L.C % 16 or L.cl else
                                                "igemm_ffma_cp_kernel" if L.dtype == "f32" else
