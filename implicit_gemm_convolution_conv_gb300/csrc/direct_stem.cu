@@ -408,20 +408,18 @@ constexpr long long kTinyOutputs = 1 << 16;
 template <typename T, int C, int S>
 __global__ void __launch_bounds__(128) direct_tiny_kernel(const StemArgs a) {
     pdl_launch_dependents();
-    // The output coordinates (32-bit: at most 65,536 outputs) before the
-    // dependency wait, which only global memory has to follow.
-    const unsigned total = (unsigned)a.N * a.OC * a.OH * a.OW;
-    const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
-    const unsigned ow = i % (unsigned)a.OW;
-    unsigned r = i / (unsigned)a.OW;
-    const unsigned oh = r % (unsigned)a.OH;
-    r /= (unsigned)a.OH;
-    const unsigned oc = r % (unsigned)a.OC;
-    const unsigned n = r / (unsigned)a.OC;
-    const T *x = static_cast<const T *>(a.x) + (size_t)n * C * a.H * a.W;
-    const T *w = static_cast<const T *>(a.w) + (size_t)oc * C * 9;
     pdl_wait();
+    const long long total = (long long)a.N * a.OC * a.OH * a.OW;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= total) return;
+    const int ow = (int)(i % a.OW);
+    long long r = i / a.OW;
+    const int oh = (int)(r % a.OH);
+    r /= a.OH;
+    const int oc = (int)(r % a.OC);
+    const int n = (int)(r / a.OC);
+    const T *x = static_cast<const T *>(a.x) + (long long)n * C * a.H * a.W;
+    const T *w = static_cast<const T *>(a.w) + (long long)oc * C * 9;
     float xv[C * 9], wv[C * 9];
 #pragma unroll
     for (int c = 0; c < C; ++c)
