@@ -169,6 +169,33 @@ def test_workspace_checks():
     assert gb.weight_packed_size(d, 2) == (gb.OK, w_pk)
 
 
+def test_workspace_holds_the_split_k_partial_sums_of_small_fp32_layers():
+    """fp32 on the CUDA-core GEMM with C % 16 == 0 and NCHW x: a layer of
+    fewer than 160 tiles of 128 x 128 splits K, and its workspace holds S
+    slices of [OC][N*OH*OW] fp32 partial sums
+    (S = min(8, K steps / 2), fewer if the slices would pass 64 MB); a
+    larger layer, a channel count not divisible by 16, channels-last x or
+    16-bit storage get none."""
+    def ws(N, C, H, W, OC, **kw):
+        d = gb.make_desc(N, C, H, W, OC, 3, 1, 1, algo=gb.ALGO_IGEMM_FFMA, w_layout=gb.W_PACKED, **kw)
+        st, n = gb.workspace_size(d, 2)
+        assert st == gb.OK
+        return n
+    # layer 3: 120 tiles, K = 9 * 64 = 576 -> 36 steps of 16 -> 8 slices of 128 x 15360 fp32
+    slices = 128 * 16 * 12 * 80 * 4
+    assert ws(16, 64, 12, 80, 128) == 8 * slices
+    # 16 channels: 9 steps -> 4 slices
+    assert ws(2, 16, 20, 30, 40) == (4 * 40 * 2 * 20 * 30 * 4 + 255) // 256 * 256
+    assert ws(64, 64, 40, 80, 128) == 0                  # 1600 tiles: no split
+    assert ws(16, 60, 12, 80, 128) == 0                  # C % 16 != 0
+    assert ws(16, 64, 12, 80, 128, channels_last=True) == 0
+    assert ws(16, 64, 12, 80, 128, dtype=gb.F16) == 0
+    # OIHW weights add the packed copy in front of the partial sums
+    d = gb.make_desc(16, 64, 12, 80, 128, 3, 1, 1, algo=gb.ALGO_IGEMM_FFMA)
+    w_pk = 9 * 64 * 128 * 4
+    assert gb.workspace_size(d, 2) == (gb.OK, (w_pk + 255) // 256 * 256 + 8 * slices)
+
+
 def test_workspace_overlapping_an_input_is_rejected():
     # The layout pass and the weight pack write the workspace while x, w and
     # b are read: a workspace over any of them is refused before any CUDA call.
