@@ -477,12 +477,39 @@ def run_ours(args):
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / reps
         hy = pipes[0][5]
+        # The host link's floor for this step on this machine: the same copies
+        # alone (H2D of x, w, b and D2H of y on two streams at once), no call.
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        _, x0, w0, b0, c0, hy0 = pipes[0]
+
+        def copies():
+            s_in.wait_stream(stream)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_in):
+                x0.copy_(hx, non_blocking=True)
+                w0.copy_(hw, non_blocking=True)
+                b0.copy_(hb, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                hy0.copy_(c0.y, non_blocking=True)
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
+        for _ in range(3):
+            copies()
+        torch.cuda.synchronize()
+        n_copy = 20
+        e0.record(stream)
+        for _ in range(n_copy):
+            copies()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        copy_ms = e0.elapsed_time(e1) / n_copy
         line["e2e"] = {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 4),
                        "unit": "TFLOP/s",
                        "h2d_bytes_per_step": hx.numel() * hx.element_size() +
                        hw.numel() * hw.element_size() + hb.numel() * 4,
                        "d2h_bytes_per_step": hy.numel() * hy.element_size(),
                        "ms_per_step": round(e2e_ms, 5),
+                       "copies_only_ms_per_step": round(copy_ms, 5),
                        "streams": n_pipe,
                        "issue": "one CUDA graph per stream: H2D x, w, b; the C-ABI call; D2H y"}
         if not args.skip_layers:
