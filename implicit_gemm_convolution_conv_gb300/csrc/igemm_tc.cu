@@ -207,17 +207,22 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         // The first ring's worth of the first tile's boxes, for operands that
         // no kernel of this call writes, start towards L2 while the previous
         // kernel finishes (L2 is where the GPU's writes become coherent, so
-        // the loads after the wait cannot see stale data). The pixel run's
-        // start is clamped into the tensor: a hint needs no zero fill.
+        // the loads after the wait cannot see stale data). An x box is
+        // prefetched at the traversal start its load uses, and only where
+        // that start lies inside the tensor in every dimension. (An im2col
+        // coordinate must lie in the traversal range [-pad, extent - 1 + pad
+        // - (k - 1)] of each dimension; a start clamped to 0 leaves that range
+        // when its upper end is negative, as for D = 1 with k = 5 and pad 2,
+        // and such a copy ends the context with an illegal instruction.)
         if (!TcElt<T>::kSplit && a.prefetch && (int)blockIdx.x < a.num_tiles) {
             const TileCoord tc = tile_coord(a, blockIdx.x);
-            const int x0 = max(tc.ow * a.stride - a.pad, 0), y0 = max(tc.oh * a.stride - a.pad, 0),
-                      z0 = max(tc.od * a.stride - a.pad_d, 0);
+            const int x0 = tc.ow * a.stride - a.pad, y0 = tc.oh * a.stride - a.pad, z0 = tc.od * a.stride - a.pad_d;
+            const bool x_inside = x0 >= 0 && y0 >= 0 && z0 >= 0;
             int cb = 0, kx = 0, ky = 0, kz = 0, tap = 0;
             for (int it = 0; it < a.stages && it < a.ksteps; ++it) {
                 const int c0 = cb * TcElt<T>::kBlk;
                 if (a.prefetch & 2) tma_prefetch_l2_3d(&tmW, c0, tc.oc0, tap);
-                if ((a.prefetch & 1) && x0 + kx < a.in_w && y0 + ky < a.in_h && z0 + kz < a.in_d)
+                if ((a.prefetch & 1) && x_inside && x0 + kx < a.in_w && y0 + ky < a.in_h && z0 + kz < a.in_d)
                     tma_prefetch_l2_im2col_5d(&tmX, c0, x0, y0, z0, tc.n, (uint16_t)kx, (uint16_t)ky,
                                               (uint16_t)kz);
                 if (++cb == a.cblocks) {

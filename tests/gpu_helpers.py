@@ -88,15 +88,21 @@ def errors(y, ref):
             "max_abs": float(np.max(np.abs(err))) if err.size else 0.0}
 
 
-def assert_close(dtype, y, ref, what=""):
+def assert_close(dtype, y, ref, what="", tf32x3_k=0):
+    """tf32x3_k: for an fp32 call forced onto the tensor cores' three TF32
+    products, its reduction length C * k^d. Beyond 1,000 products (where
+    AUTO takes the exact CUDA-core GEMM instead) that path's error grows
+    with the reduction, and it is held to the fp32 bars scaled by K / 1000,
+    its documented bound (include/gbconv.h)."""
     y = np.asarray(y, np.float64).ravel()
     ref = np.asarray(ref, np.float64).ravel()
     assert y.shape == ref.shape
     assert np.isfinite(y).all(), f"{what}: non-finite output"
     e = errors(y, ref)
     if dtype == "f32":
-        assert e["rel_l2"] <= 1e-5, (what, e)
-        assert e["max_abs"] <= 1e-4, (what, e)
+        scale = max(1.0, tf32x3_k / 1000.0)
+        assert e["rel_l2"] <= 1e-5 * scale, (what, e)
+        assert e["max_abs"] <= 1e-4 * scale, (what, e)
     elif dtype == "f16":
         assert e["rel_l2"] <= 1e-3, (what, e)
         bad = np.abs(y - ref) > 2.0 ** -10 * np.abs(ref) + 3e-4

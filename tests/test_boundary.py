@@ -236,6 +236,23 @@ def test_shapes_and_algorithm_of_the_five_layers(idx):
     assert algo == expect, gb.algo_name(algo)
 
 
+def test_auto_keeps_long_fp32_reductions_on_the_cuda_cores():
+    """fp32 layers go to the tensor cores' three TF32 products only while
+    the reduction C * k^d is at most 1,000 products (the three-product
+    error grows with it); longer ones, NCHW or channels-last, go to the
+    exact-fp32 CUDA-core GEMM. 16-bit storage stays on the tensor cores."""
+    pick = lambda **kw: gb.select_algo(_desc(**kw), 2)[1]
+    assert pick(C=64, OC=128, H=12, W=80, k=3, pad=1) == gb.ALGO_IGEMM_TC          # 576
+    assert pick(C=111, OC=128, H=12, W=80, k=3, pad=1) == gb.ALGO_IGEMM_TC         # 999
+    assert pick(C=112, OC=128, H=12, W=80, k=3, pad=1) == gb.ALGO_IGEMM_FFMA       # 1008
+    assert pick(C=48, OC=128, H=12, W=80, k=5, pad=2) == gb.ALGO_IGEMM_FFMA        # 1200
+    assert pick(C=256, OC=256, H=32, W=32, k=3, pad=1, dtype=gb.F16) == gb.ALGO_IGEMM_TC
+    d = gb.make_desc(1, 128, 32, 32, 64, 3, 1, 1, channels_last=True)
+    assert gb.select_algo(d, 2) == (gb.OK, gb.ALGO_IGEMM_FFMA)
+    d = gb.make_desc(1, 128, 32, 32, 64, 3, 1, 1, D=4)                             # 3456 in 3D
+    assert gb.select_algo(d, 3) == (gb.OK, gb.ALGO_IGEMM_FFMA)
+
+
 def test_auto_picks_tensor_core_stem_for_fp32_stems():
     """fp32 3x3 stems (C <= 4) with 16 to 128 output channels go to the
     tensor-core stem; narrower and wider ones, other dtypes, C > 4 and the

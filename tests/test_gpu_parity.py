@@ -266,7 +266,8 @@ def test_sweep(algo, L):
     inp = synthetic.make_inputs(L)
     y, conv = run(inp, algo=algo)
     assert conv.algo == algo
-    assert_close(L.dtype, y, reference(inp), str(L))
+    tf32x3 = L.C * L.k ** L.ndim if (L.dtype == "f32" and algo == A_TC) else 0
+    assert_close(L.dtype, y, reference(inp), str(L), tf32x3_k=tf32x3)
 
 
 # -------------------------------------------------- packing, determinism
