@@ -102,6 +102,36 @@ def test_stem_tensor_cores_many_tiles_per_group(OC, W):
     assert_close(L.dtype, y, reference(inp), L.name)
 
 
+# Stems of 720 and 800 tiles of 2 rows x 64 pixels (five or six tiles per SM
+# on 152 SMs, so one or two of a CTA's four groups run a second tile).
+STEMS_5_6 = [
+    # 720 tiles; OC 24 (padded to 32), no bias
+    synthetic.Layer("stem_720_tiles_oc24", N=1, C=2, H=288, W=320, OC=24, k=3, pad=1, stride=1, dtype="f32",
+                    x_dist="u01", w_dist="he", b_dist="none", seed=301),
+    # 800 tiles, stride 3 (the widest halo box), OC 16, ReLU
+    synthetic.Layer("stem_800_tiles_s3", N=1, C=3, H=960, W=960, OC=16, k=3, pad=1, stride=3, dtype="f32",
+                    relu=True, x_dist="u01", w_dist="he", b_dist="u01_1", seed=302),
+    # 800 tiles over four images, one input channel, a 16-pixel last column tile
+    synthetic.Layer("stem_800_tiles_c1_ragged", N=4, C=1, H=200, W=416, OC=8, k=3, pad=1, stride=2, dtype="f32",
+                    relu=True, x_dist="u01", w_dist="he", b_dist="u01_1", seed=303),
+    # 720 tiles, an odd number of output rows (the last row pair is half empty)
+    synthetic.Layer("stem_720_tiles_odd_rows", N=1, C=3, H=574, W=640, OC=32, k=3, pad=1, stride=2, dtype="f32",
+                    relu=True, x_dist="u01", w_dist="he", b_dist="u01_1", seed=304),
+]
+
+
+@pytest.mark.parametrize("L", STEMS_5_6, ids=lambda L: L.name)
+def test_stem_tensor_cores_five_or_six_tiles_per_sm(L):
+    """The tensor-core stem at tile counts near the 640 x 640 stem's: ragged
+    channel counts, no bias, stride 3 (the widest halo box), one input
+    channel, a part-width last tile and a half-empty last row pair. Every
+    output is checked."""
+    inp = synthetic.make_inputs(L)
+    y, conv = run(inp, algo=A_DTC)
+    assert conv.algo == A_DTC
+    assert_close(L.dtype, y, reference(inp), L.name)
+
+
 @pytest.mark.parametrize("idx,dtype", [(4, "f16"), (5, "f16"), (4, "bf16")])
 def test_tensor_core_layer_full_output(idx, dtype):
     """The wide dense layer (f16, bf16) and the video-VAE Convolution3D at
