@@ -556,10 +556,22 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 }
             };
             // Chunks grp, grp + 2, ...: the next chunk's TMEM load is in
-            // flight while the current one is converted and stored.
+            // flight while the current one is converted and stored. A CTA
+            // with a single tile has nothing for its epilogue to hide under,
+            // and there a TMEM load in flight slows the staging stores of the
+            // chunk before it (measured on the 128 x 128 x 256-channel layer:
+            // 1.76 against 1.57 us per epilogue), so it loads each chunk when
+            // it needs it.
             const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.NP);
             uint32_t va[32], vb[32];
             int ch = grp;
+            if (a.single_tile) {
+                for (; ch < nchunks; ch += 2) {
+                    tmem_ld32(tl + (uint32_t)(ch * kColChunk), va);
+                    tmem_ld_wait();
+                    store_chunk(va, ch);
+                }
+            }
             if (ch < nchunks) tmem_ld32(tl + (uint32_t)(ch * kColChunk), va);
             while (ch < nchunks) {
                 tmem_ld_wait();
