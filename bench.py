@@ -216,6 +216,9 @@ def recorded_traffic(kernel_file, key):
 ROTATE_BYTES = 256 << 20     # > 2 x L2: a set is cold when it comes round again
 
 
+GRAPH_CALLS = 64     # calls per captured graph, at least (see Rotation.graphs)
+
+
 class Rotation:
     """R copies of the layer's input/output buffers used in turn, so that no
     step finds its x or y in L2 (R x set bytes >= 256 MiB); steps are
@@ -241,10 +244,17 @@ class Rotation:
         self.i += 1
 
     def graphs(self, steps):
-        """CUDA graphs whose replay runs exactly `steps` calls in turn."""
+        """CUDA graphs whose replay runs exactly `steps` calls in turn. A graph
+        holds a whole number of rounds over the copies and at least
+        GRAPH_CALLS calls (fewer only when `steps` is smaller): consecutive
+        calls inside a graph overlap through programmatic dependent launch,
+        while a boundary between two replays costs a graph launch, which one
+        graph per round (a single call for an L2-resident layer) would add
+        to every few calls."""
         torch = self.torch
         r = len(self.convs)
-        full, tail = divmod(steps, r)
+        per = min(steps, r * -(-GRAPH_CALLS // r))
+        full, tail = divmod(steps, per)
         out = []
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -252,10 +262,10 @@ class Rotation:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
                 for j in range(n):
-                    self.convs[j]()
+                    self.convs[j % r]()
             return g
         if full:
-            g = capture(r)
+            g = capture(per)
             out += [g] * full
         if tail:
             out.append(capture(tail))
