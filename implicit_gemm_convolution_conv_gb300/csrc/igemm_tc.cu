@@ -610,7 +610,11 @@ igemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 // bytes), stores 16-byte vectors of 8 channels (8 lanes = one position's 128
 // contiguous bytes). The shared tile keeps a channel's row of positions in
 // 16-byte chunks whose index is XOR-ed with (channel / 8) % 8, so the column
-// reads of the store phase hit 16 different banks per warp.
+// reads of the store phase hit 16 different banks per warp. With 16-byte
+// rows (S % 8 == 0, x aligned) the loads are cp.async copies into the tile,
+// which hold no registers: 32 registers a thread, 7 CTAs per SM (4 with the
+// loads staged through registers; the video-VAE Convolution3D's 1,200
+// blocks then took two full waves).
 constexpr int kClC = 64, kClS = 256;
 template <typename T, bool VEC>
 __device__ __forceinline__ void to_channels_last_block(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp,
@@ -621,27 +625,44 @@ __device__ __forceinline__ void to_channels_last_block(const T *__restrict__ x, 
     const T *xn = x + (int64_t)n * C * S;
     T *xcn = xc + (int64_t)n * S * Cp;
     constexpr int kIter = kClC * kClS / 8 / 256;
-    uint4 buf[kIter];
+    if constexpr (VEC) {
+        // 16-byte copies straight into the swizzled tile (S % 8 == 0 and x
+        // 16-byte aligned: a vector is whole or past the tensor, where the
+        // copy reads nothing and zero-fills); all of a thread's copies are in
+        // flight at once and hold no registers.
+        const uint32_t tbase = smem_u32(&tile[0][0]);
 #pragma unroll
-    for (int i = 0; i < kIter; ++i) {
-        const int v = threadIdx.x + 256 * i;
-        const int cl = v / (kClS / 8), p8 = v % (kClS / 8);
-        const int cc = c0 + cl;
-        const int64_t s = s0 + p8 * 8;
-        if (VEC && cc < C && s + 8 <= S) {
-            buf[i] = __ldg(reinterpret_cast<const uint4 *>(xn + (int64_t)cc * S + s));
-        } else {
+        for (int i = 0; i < kIter; ++i) {
+            const int v = threadIdx.x + 256 * i;
+            const int cl = v / (kClS / 8), p8 = v % (kClS / 8);
+            const int cc = c0 + cl;
+            const int64_t s = s0 + p8 * 8;
+            const bool in = cc < C && s < S;
+            const T *src = in ? xn + (int64_t)cc * S + s : xn;
+            const uint32_t dst = tbase + (uint32_t)(cl * kClS + (p8 ^ ((cl >> 3) & 7)) * 8) * (uint32_t)sizeof(T);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(in ? 16 : 0)
+                         : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else {
+        uint4 buf[kIter];
+#pragma unroll
+        for (int i = 0; i < kIter; ++i) {
+            const int v = threadIdx.x + 256 * i;
+            const int cl = v / (kClS / 8), p8 = v % (kClS / 8);
+            const int cc = c0 + cl;
+            const int64_t s = s0 + p8 * 8;
             alignas(16) T e[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) e[j] = (cc < C && s + j < S) ? xn[(int64_t)cc * S + s + j] : T(0.0f);
             buf[i] = *reinterpret_cast<const uint4 *>(e);
         }
-    }
 #pragma unroll
-    for (int i = 0; i < kIter; ++i) {
-        const int v = threadIdx.x + 256 * i;
-        const int cl = v / (kClS / 8), p8 = v % (kClS / 8);
-        *reinterpret_cast<uint4 *>(&tile[cl][(p8 ^ ((cl >> 3) & 7)) * 8]) = buf[i];
+        for (int i = 0; i < kIter; ++i) {
+            const int v = threadIdx.x + 256 * i;
+            const int cl = v / (kClS / 8), p8 = v % (kClS / 8);
+            *reinterpret_cast<uint4 *>(&tile[cl][(p8 ^ ((cl >> 3) & 7)) * 8]) = buf[i];
+        }
     }
     __syncthreads();
 #pragma unroll
@@ -660,7 +681,7 @@ __device__ __forceinline__ void to_channels_last_block(const T *__restrict__ x, 
     }
 }
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(256, 7)
 to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S) {
     __shared__ __align__(16) T tile[kClC][kClS];
     pdl_launch_dependents();   // the GEMM behind launches once every CTA here has started
@@ -669,11 +690,11 @@ to_channels_last_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int 
 }
 
 // wp[tap][oc][cp] = w[oc][c][tap] for c < C, zero for C <= cp < Cp. A CTA
-// handles ocpb (1 to 8, about 512 16-byte vectors' worth: pack_oc_block)
+// handles ocpb (1 to 8, at most 512 16-byte vectors' worth: pack_oc_block)
 // output channels, 64 channels and up to 32 taps. When all taps
 // fit and the block is whole, each output channel's part of w is one
 // contiguous run of 64 * taps elements, read as 16-byte vectors; a thread
-// issues all of its loads (at most 8) before it writes any to shared memory,
+// issues all of its loads (at most 2) before it writes any to shared memory,
 // so the CTA waits for one memory round trip. Other blocks read element by
 // element in batches of 8 loads. Each (tap, output channel) pair's 64
 // channels then leave as one 128-byte run of wp.
@@ -697,7 +718,8 @@ __device__ __forceinline__ void pack_tc_block(const T *__restrict__ w, T *__rest
                      ((int64_t)C * taps) % 8 == 0 && ((uintptr_t)w % 16) == 0;
     if (vec) {
         const int vpr = kPkC * taps / 8;                      // vectors per output channel's run
-        constexpr int kMaxV = kPkOc * kPkC * kPkT / 8 / 256;  // 8
+        // pack_oc_block keeps a block within 512 vectors: two per thread
+        constexpr int kMaxV = 512 / 256;
         uint4 buf[kMaxV];
 #pragma unroll
         for (int k = 0; k < kMaxV; ++k) {
@@ -776,8 +798,13 @@ constexpr size_t prep_tile_bytes() {
     return sizeof(T) * kClC * kClS > sizeof(T) * kPkOc * kPkC * (kPkT + 1) ? sizeof(T) * kClC * kClS
                                                                           : sizeof(T) * kPkOc * kPkC * (kPkT + 1);
 }
-template <typename T, bool VEC>
-__global__ void __launch_bounds__(256, 4)
+// MINB: resident CTAs per SM the registers are sized for. A grid that fits
+// on the SMs at 4 CTAs each keeps 64 registers (the pack blocks' loads all in
+// flight, no spills); a larger one (the video-VAE Convolution3D's 1,328
+// blocks) runs 6 per SM, two waves instead of three (measured: its call
+// 94.9 -> 90.5 us), at the cost of a few spilled registers in the pack blocks.
+template <typename T, bool VEC, int MINB>
+__global__ void __launch_bounds__(256, MINB)
 prep_tc_kernel(const T *__restrict__ x, T *__restrict__ xc, int C, int Cp, int64_t S, int clx, int cly,
                const T *__restrict__ w, T *__restrict__ wp, int OC, int taps, int ocpb, int pkx, int pky, int npk,
                int nlay) {
@@ -1326,7 +1353,12 @@ cudaError_t launch_prep_tc_typed(const Problem &p, const void *w, void *wp, cons
     const int64_t total = npk + nlay;
     if (total > 0x7FFFFFFF) return cudaErrorNotSupported;   // caller falls back to two launches
     const bool vec = (S % 8 == 0) && ((uintptr_t)x % 16 == 0);
-    auto kern = vec ? prep_tc_kernel<T, true> : prep_tc_kernel<T, false>;
+    DevInfo info;
+    const cudaError_t e = dev_info(&info);
+    if (e != cudaSuccess) return e;
+    const bool big = total > 4ll * info.sms;
+    auto kern = vec ? (big ? prep_tc_kernel<T, true, 6> : prep_tc_kernel<T, true, 4>)
+                    : (big ? prep_tc_kernel<T, false, 6> : prep_tc_kernel<T, false, 4>);
     return launch_pdl(kern, dim3((unsigned)total), dim3(256), 0, s, static_cast<const T *>(x), static_cast<T *>(xc),
                       p.C, Cp, S, (int)clx, (int)cly, static_cast<const T *>(w), static_cast<T *>(wp), p.OC, p.taps,
                       ocpb, (int)pkx, (int)pky, (int)npk, (int)nlay);
