@@ -219,6 +219,16 @@ ROTATE_BYTES = 256 << 20     # > 2 x L2: a set is cold when it comes round again
 GRAPH_CALLS = 64     # calls per captured graph, at least (see Rotation.graphs)
 
 
+def graph_plan(steps, copies):
+    """How Rotation.graphs splits `steps` calls over `copies` buffer copies:
+    (calls per graph, replays of it, calls in a last shorter graph). A graph
+    holds whole rounds over the copies and at least GRAPH_CALLS calls, or all
+    the steps when there are fewer."""
+    per = min(steps, copies * -(-GRAPH_CALLS // copies))
+    full, tail = divmod(steps, per)
+    return per, full, tail
+
+
 class Rotation:
     """R copies of the layer's input/output buffers used in turn, so that no
     step finds its x or y in L2 (R x set bytes >= 256 MiB); steps are
@@ -253,8 +263,7 @@ class Rotation:
         to every few calls."""
         torch = self.torch
         r = len(self.convs)
-        per = min(steps, r * -(-GRAPH_CALLS // r))
-        full, tail = divmod(steps, per)
+        per, full, tail = graph_plan(steps, r)
         out = []
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
