@@ -1,12 +1,15 @@
 """GPU parity on seeded random problems: whatever kernel AUTO picks, and every
 other algorithm that accepts the descriptor, against the fp64 oracle.
 
-48 problems are drawn once from a fixed seed: conv2d or conv3d, f32 / f16 /
-bf16 storage, NCHW or channels-last activations, 1-3 images, 1-80 input and
-1-150 output channels, 1-40 pixels per side, k 1/3/5, pad 0..k/2+1, stride
-1-3, causal or symmetric frames, bias or none, ReLU or none. Problems whose
-output would be empty, or that need more than 2e8 products (the oracle's
-budget), are redrawn. Each one runs through AUTO and through
+Two generators, each with fixed seeds:
+- 3 x 48 problems: conv2d or conv3d, f32 / f16 / bf16 storage, NCHW or
+  channels-last activations, 1-3 images, 1-80 input and 1-150 output
+  channels, 1-40 pixels per side, k 1/3/5, pad 0..k/2+1, stride 1-3, causal
+  or symmetric frames, bias or none, ReLU or none (at most 2e8 products);
+- 64 wider problems: 1-4 images, 1-300 input and output channels, 1-96
+  pixels per side, up to 6 frames, k 1/3/5/7 (at most 1e9 products).
+Problems whose output would be empty, or that exceed the oracle's product
+budget, are redrawn. Each one runs through AUTO and through
 each algorithm forced (DIRECT, IGEMM_FFMA, IGEMM_TC, DIRECT_TC) that the
 library accepts for it, so the kernel families meet shapes no hand-written
 case chose; the tolerances are the dtype's (gpu_helpers), with fp32 forced
@@ -51,7 +54,31 @@ def _draw(count=48, seed=2026):
     return out
 
 
-PROBLEMS = _draw()
+def _draw_wide(count=64, seed=101):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    while len(out) < count:
+        ndim = int(rng.choice([2, 2, 3]))
+        k = int(rng.choice([1, 3, 3, 5, 7]))
+        pad = int(rng.integers(0, k // 2 + 2))
+        stride = int(rng.integers(1, 4))
+        dtype = str(rng.choice(["f32", "f16", "bf16"]))
+        C = int(rng.choice([int(rng.integers(1, 9)), int(rng.integers(8, 97)), int(rng.integers(96, 301))]))
+        OC = int(rng.choice([int(rng.integers(1, 65)), int(rng.integers(64, 301))]))
+        L = synthetic.Layer(
+            f"wide{len(out)}", N=int(rng.integers(1, 5)), C=C,
+            D=int(rng.integers(1, 7)) if ndim == 3 else 1,
+            H=int(rng.integers(1, 97)), W=int(rng.integers(1, 97)),
+            OC=OC, k=k, pad=pad, stride=stride, dtype=dtype,
+            relu=bool(rng.integers(0, 2)), ndim=ndim, x_dist="n01", w_dist="he",
+            b_dist=str(rng.choice(["u005", "none"])), seed=int(rng.integers(0, 1 << 30)),
+            tpad=int(rng.choice([0, 1])) if ndim == 3 else 0, cl=bool(rng.integers(0, 2)))
+        if min(L.out_dims()) >= 1 and L.flops() <= 1e9:
+            out.append(L)
+    return out
+
+
+PROBLEMS = _draw() + _draw(48, 7) + _draw(48, 11) + _draw_wide()
 
 
 def _accepts(L, algo):
